@@ -1,0 +1,17 @@
+"""CPU oracle of the spec-tree step: test infrastructure, not product code.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.
+"""
+from .bastion_oracle import (  # noqa: F401
+    Tree,
+    accept,
+    attend,
+    context_kv,
+    marginals,
+    path_to_root,
+    stack_trees,
+    topk_softmax,
+    tree_attention,
+    tree_build,
+)

@@ -1,0 +1,373 @@
+"""CPU oracle for the BASTION spec-tree step (test infrastructure only).
+
+This module is the correctness reference for the CUDA library.  Only the test
+suite, the smoke check and the benchmark's CPU-baseline leg may import it; the
+product path never calls it and has no CPU fallback.  It imports numpy and
+nothing from the CUDA package; the two share no code.
+
+It is deliberately plain and slow: float64 arithmetic, straightforward loops,
+library primitives (exp, stable sort, argmax, dot products) as single steps and
+no blocking, fusion or reordering beyond what the definitions state.
+
+Sources (cited by page title and section):
+  [B] "Bastion: Budget-Aware Speculative Decoding with Tree-structured Block
+      Diffusion Drafting", explainer page gist.science/de/paper/2605.29727
+      (German) and its Spanish twin gist.science/es/paper/2605.29727.
+      Section "Methodik: BASTION":
+        §1 "Baumgestützte block-diffusionsbasierte Drafting": one drafter pass
+           gives per-position marginals q_k(.); candidates at different
+           positions combine freely into a prefix tree ("Randverteilungs-
+           Unabhängigkeit"); path score rho(i) = prod_{k=1}^{d(i)} q_k(x_ik).
+        §2 "Akzeptanz-Surrogat und Best-First-Erweiterung": A_hat(T) = sum of
+           rho over the tree; best-first adds the valid node of highest rho.
+        §3 "Hardwarebewusster Online-Budget-Controller": grow the tree until
+           S(N) = A_hat(T_N) * L_AR / C(N) starts to fall.
+      Section "Experimentelle Ergebnisse": greedy decoding (temperature 0).
+      Section "Problemstellung": the target verifies the drafted tokens in one
+      parallel pass ("baumgestützte Verifizierung" under "Akzeptanzlänge").
+
+Readings where the pages are silent (each is listed in the design notes):
+  * the root is node 0 of the tree and counts in N and in A_hat, rho(root) = 1
+    (the empty product of §1);
+  * children of a depth-d node are the top-k tokens of position d+1;
+  * order: higher rho first, then lower token id, then lower parent index;
+    rho is compared through its log, key = (fp32 sum of the path's logits,
+    accumulated root to leaf) - (sum of the per-position log-normalisers),
+    so exact ties at equal depth stay exact and the decision is taken in the
+    kernel's precision; the reported rho uses the exact float64 path sum;
+  * C(N) is a table indexed by N = 1..n_max; fixed budget when it is absent;
+  * the controller pops unconditionally up to n_min, then stops at the first
+    n with S(n+1) < S(n) (strict);
+  * tree attention: node i attends to every context key and to the tree keys
+    of its root-to-i path, self included, softmax(q.k * scale);
+  * acceptance: per-node argmax (lowest id on ties), walk from the root to the
+    child whose token equals the parent's argmax; accepted length counts the
+    accepted draft tokens, the bonus is the argmax where the walk stops.
+
+Every function here is pinned by CPU tests against closed forms, brute force,
+library routines or worked examples; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+
+# --------------------------------------------------------------------------
+# Stage 1: per-position marginals and top-k   ([B] Methodik §1)
+# --------------------------------------------------------------------------
+
+
+def marginals(logits_row: np.ndarray):
+    """Softmax of one drafter position over the whole vocabulary, temperature 1.
+
+    q(v) = exp(l_v - m) / sum_u exp(l_u - m), m = max_u l_u;  also returns
+    lse = m + log sum_u exp(l_u - m) = log sum_u exp(l_u).
+    [B] Methodik §1: the drafter yields per-position marginals q_k(.).
+    """
+    l = np.asarray(logits_row, dtype=np.float64)
+    m = l.max()
+    e = np.exp(l - m)
+    z = e.sum()
+    return e / z, m + math.log(z)
+
+
+def topk_softmax(logits: np.ndarray, k: int):
+    """Top-k candidates of every drafter row.
+
+    ``logits`` is [R, V] (any float dtype; values are taken exactly).  Returns
+    ids [R,k] int32, lg [R,k] float64 (the logits), q [R,k] float64 and
+    lse [R] float64.  Candidates are ordered by logit descending, then token id
+    ascending (a stable sort of -logit), which is the order of q as well.
+    """
+    L = np.asarray(logits, dtype=np.float64)
+    R, V = L.shape
+    ids = np.empty((R, k), dtype=np.int32)
+    lg = np.empty((R, k), dtype=np.float64)
+    q = np.empty((R, k), dtype=np.float64)
+    lse = np.empty(R, dtype=np.float64)
+    for r in range(R):
+        q_full, lse[r] = marginals(L[r])
+        order = np.argsort(-L[r], kind="stable")[:k]
+        ids[r] = order
+        lg[r] = L[r, order]
+        q[r] = q_full[order]
+    return ids, lg, q, lse
+
+
+# --------------------------------------------------------------------------
+# Stage 2: best-first prefix tree with the S(N) budget stop
+#          ([B] Methodik §1 "Pfad-Bewertung", §2, §3)
+# --------------------------------------------------------------------------
+
+
+@dataclass
+class Tree:
+    n: int
+    parent: np.ndarray      # [n_max] int32, -1 for the root and unused rows
+    token: np.ndarray       # [n_max] int32
+    depth: np.ndarray       # [n_max] int32
+    pos: np.ndarray         # [n_max] int32  (ctx_len + depth)
+    rho: np.ndarray         # [n_max] float64
+    mask: np.ndarray        # [n_max, W] uint64 ancestor-or-self bits
+    ahat: float             # A_hat(T_n)
+    S: float                # S(n)
+    S_curve: np.ndarray     # [n_max] float64, S(j+1) for j < n, 0 beyond
+    key: np.ndarray         # [n_max] float64 log rho of each node (diagnostic)
+    min_gap: float          # smallest relative gap of an inexact decision
+
+
+def _build_one(ids, lg, lse, root_tok, ctx_len, n_min, n_max, C, L_AR) -> Tree:
+    K, k = ids.shape
+    # prefix of log-normalisers: P[d] = sum_{t=1..d} lse_t, so that
+    # log rho(i) = sum_{t<=d} l_t(x_t) - P[d]   (log of the product in §1)
+    P = np.zeros(K + 1, dtype=np.float64)
+    for t in range(1, K + 1):
+        P[t] = P[t - 1] + float(lse[t - 1])
+
+    par = [-1]
+    tok = [int(root_tok)]
+    dep = [0]
+    S32 = [np.float32(0.0)]          # fp32 logit sum along the path (decisions)
+    S64 = [0.0]                      # exact float64 logit sum along the path (reported rho)
+    key = [0.0]                      # log rho(root) = log 1
+    rho = [1.0]
+
+    # frontier: every child of every tree node not yet in the tree
+    f_key: list = []
+    f_tok: list = []
+    f_par: list = []
+    f_dep: list = []
+    f_S: list = []
+    f_S64: list = []
+
+    def offer_children(i: int) -> None:
+        d = dep[i]
+        if d >= K:
+            return
+        for j in range(k):
+            s = np.float32(S32[i] + np.float32(lg[d, j]))    # position d+1
+            f_key.append(float(s) - P[d + 1])
+            f_tok.append(int(ids[d, j]))
+            f_par.append(i)
+            f_dep.append(d + 1)
+            f_S.append(s)
+            f_S64.append(S64[i] + float(lg[d, j]))
+
+    offer_children(0)
+    ahat = [1.0]                     # A_hat after n nodes, n = 1 (root only)
+    min_gap = math.inf
+
+    def best_index() -> int:
+        # highest rho (key), then lowest token id, then lowest parent index
+        order = np.lexsort((np.asarray(f_par), np.asarray(f_tok), -np.asarray(f_key)))
+        return int(order[0])
+
+    def decision_gap(b: int) -> float:
+        # relative rho gap between the chosen candidate and every other one
+        # whose order is not an exact tie (same depth, same fp32 logit sum)
+        fk = np.asarray(f_key)
+        exact_tie = (np.asarray(f_dep) == f_dep[b]) & (np.asarray(f_S, dtype=np.float32) == f_S[b])
+        others = fk[~exact_tie]
+        if others.size == 0:
+            return math.inf
+        return 1.0 - math.exp(min(0.0, float(others.max()) - f_key[b]))
+
+    while len(par) < n_max and f_key:
+        n = len(par)
+        b = best_index()
+        min_gap = min(min_gap, decision_gap(b))
+        rho_next = math.exp(f_S64[b] - P[f_dep[b]])
+        if C is not None and n >= n_min:
+            s_now = ahat[-1] * L_AR / float(C[n])
+            s_next = (ahat[-1] + rho_next) * L_AR / float(C[n + 1])
+            min_gap = min(min_gap, abs(s_next - s_now) / max(s_now, s_next))
+            if s_next < s_now:       # S(N) begins to fall: stop (§3)
+                break
+        # pop candidate b into the tree
+        par.append(f_par[b])
+        tok.append(f_tok[b])
+        dep.append(f_dep[b])
+        S32.append(f_S[b])
+        S64.append(f_S64[b])
+        key.append(f_key[b])
+        rho.append(rho_next)
+        ahat.append(ahat[-1] + rho_next)
+        for lst in (f_key, f_tok, f_par, f_dep, f_S, f_S64):
+            del lst[b]
+        offer_children(len(par) - 1)
+
+    n = len(par)
+    W = (n_max + 63) // 64
+    out_par = np.full(n_max, -1, dtype=np.int32)
+    out_tok = np.full(n_max, -1, dtype=np.int32)
+    out_dep = np.full(n_max, -1, dtype=np.int32)
+    out_pos = np.full(n_max, -1, dtype=np.int32)
+    out_rho = np.zeros(n_max, dtype=np.float64)
+    out_key = np.zeros(n_max, dtype=np.float64)
+    mask = np.zeros((n_max, W), dtype=np.uint64)
+    S_curve = np.zeros(n_max, dtype=np.float64)
+    for i in range(n):
+        out_par[i], out_tok[i], out_dep[i] = par[i], tok[i], dep[i]
+        out_pos[i] = int(ctx_len) + dep[i]
+        out_rho[i] = rho[i]
+        out_key[i] = key[i]
+        j = i
+        while j >= 0:                # ancestor-or-self bits
+            mask[i, j // 64] |= np.uint64(1) << np.uint64(j % 64)
+            j = par[j]
+        c = 1.0 if C is None else float(C[i + 1])
+        S_curve[i] = ahat[i] * L_AR / c
+    return Tree(n=n, parent=out_par, token=out_tok, depth=out_dep, pos=out_pos, rho=out_rho,
+                mask=mask, ahat=ahat[n - 1], S=S_curve[n - 1], S_curve=S_curve, key=out_key,
+                min_gap=min_gap)
+
+
+def tree_build(ids, lg, lse, root_tok, ctx_len, n_min: int, n_max: int,
+               C: Optional[np.ndarray], L_AR: float) -> list:
+    """Best-first tree of every request.
+
+    ids/lg are [B, K, k] (top-k of each position, in stage-1 order), lse is
+    [B, K].  ``C`` is the latency table C[0..n_max] (entry n is C(n)) or None for
+    a fixed budget (then S(n) is reported with C = 1).  Returns one Tree per
+    request.
+    """
+    ids = np.asarray(ids)
+    lg = np.asarray(lg, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    return [_build_one(ids[b], lg[b], lse[b], root_tok[b], ctx_len[b], n_min, n_max, C, L_AR)
+            for b in range(ids.shape[0])]
+
+
+def stack_trees(trees: Sequence[Tree]) -> dict:
+    """Batch the per-request trees into [B, ...] arrays."""
+    return {
+        "n": np.array([t.n for t in trees], dtype=np.int32),
+        "parent": np.stack([t.parent for t in trees]),
+        "token": np.stack([t.token for t in trees]),
+        "depth": np.stack([t.depth for t in trees]),
+        "pos": np.stack([t.pos for t in trees]),
+        "rho": np.stack([t.rho for t in trees]),
+        "mask": np.stack([t.mask for t in trees]),
+        "ahat": np.array([t.ahat for t in trees]),
+        "S": np.array([t.S for t in trees]),
+        "S_curve": np.stack([t.S_curve for t in trees]),
+        "min_gap": min(t.min_gap for t in trees),
+    }
+
+
+# --------------------------------------------------------------------------
+# Stage 3: tree-masked verification attention   ([B] Problemstellung,
+#          "baumgestützte Verifizierung")
+# --------------------------------------------------------------------------
+
+
+def path_to_root(parent: np.ndarray, i: int) -> list:
+    """Node indices root -> i (depth order)."""
+    p = []
+    while i >= 0:
+        p.append(i)
+        i = int(parent[i])
+    return p[::-1]
+
+
+def context_kv(k_ctx, v_ctx, block_table, b: int, kvh: int, L: int, page_size: int):
+    """The first L context keys/values of request b, KV head kvh, as float64."""
+    if block_table is None:
+        return (np.asarray(k_ctx[b, kvh, :L], dtype=np.float64),
+                np.asarray(v_ctx[b, kvh, :L], dtype=np.float64))
+    pages = [int(block_table[b, t // page_size]) for t in range(0, L, page_size)]
+    kk = np.concatenate([np.asarray(k_ctx[p, kvh], dtype=np.float64) for p in pages])[:L]
+    vv = np.concatenate([np.asarray(v_ctx[p, kvh], dtype=np.float64) for p in pages])[:L]
+    return kk, vv
+
+
+def attend(qv: np.ndarray, keys: np.ndarray, values: np.ndarray, scale: float) -> np.ndarray:
+    """softmax(keys . q * scale) . values in float64 (one query row)."""
+    s = keys @ np.asarray(qv, dtype=np.float64) * scale
+    m = s.max()
+    p = np.exp(s - m)
+    return (p @ values) / p.sum()
+
+
+def tree_attention(q, k_tree, v_tree, k_ctx, v_ctx, ctx_len, parent, n, Hkv: int, scale: float,
+                   block_table=None, page_size: int = 16, rows=None) -> np.ndarray:
+    """Attention of every tree node over context ∪ its root path.
+
+    q [B, n_max, Hq, d]; k_tree/v_tree [B, n_max, Hkv, d]; k_ctx/v_ctx as
+    contiguous [B, Hkv, L, d] or paged [P, Hkv, page, d] with block_table.
+    For node i < n[b] and query head h (KV head h // (Hq/Hkv)) the key list is
+    context positions 0..ctx_len[b]-1 followed by the tree nodes on the path
+    root -> i.  Returns [B, n_max, Hq, d] float64 with NaN for rows not computed.
+    ``rows`` optionally restricts the work to a list of (b, i, h).
+    """
+    B, N, Hq, d = q.shape
+    g = Hq // Hkv
+    out = np.full((B, N, Hq, d), np.nan, dtype=np.float64)
+    if rows is None:
+        rows = [(b, i, h) for b in range(B) for i in range(int(n[b])) for h in range(Hq)]
+    cache = {}
+    for (b, i, h) in rows:
+        kvh = h // g
+        if (b, kvh) not in cache:
+            cache.clear()
+            cache[(b, kvh)] = context_kv(k_ctx, v_ctx, block_table, b, kvh, int(ctx_len[b]), page_size)
+        kc, vc = cache[(b, kvh)]
+        path = path_to_root(parent[b], i)
+        kt = np.asarray(k_tree[b, path, kvh], dtype=np.float64)
+        vt = np.asarray(v_tree[b, path, kvh], dtype=np.float64)
+        keys = np.concatenate([kc, kt])
+        values = np.concatenate([vc, vt])
+        out[b, i, h] = attend(q[b, i, h], keys, values, scale)
+    return out
+
+
+# --------------------------------------------------------------------------
+# Stage 4: greedy acceptance   ([B] Experimentelle Ergebnisse: temperature 0;
+#          Akzeptanzlänge)
+# --------------------------------------------------------------------------
+
+
+def accept(target, n, parent, token, K: int):
+    """Greedy verification of every request's tree.
+
+    target [B, n_max, V] (values taken exactly).  a_i = argmax_v target[b,i,v]
+    (lowest id on ties) for i < n[b].  Starting at the root, move to the child
+    whose token equals a_u; stop when there is none, the bonus token is a_u.
+    Returns acc_len [B], acc_nodes [B, K+1] (root first, -1 padded),
+    acc_tok [B, K+1] (accepted draft tokens then the bonus, -1 padded),
+    bonus [B] and argmax [B, n_max] (-1 for rows >= n[b]).
+    """
+    B, N, V = target.shape
+    acc_len = np.zeros(B, dtype=np.int32)
+    acc_nodes = np.full((B, K + 1), -1, dtype=np.int32)
+    acc_tok = np.full((B, K + 1), -1, dtype=np.int32)
+    bonus = np.zeros(B, dtype=np.int32)
+    amax = np.full((B, N), -1, dtype=np.int32)
+    for b in range(B):
+        nb = int(n[b])
+        for i in range(nb):
+            amax[b, i] = int(np.argmax(np.asarray(target[b, i], dtype=np.float64)))
+        u = 0
+        path = [0]
+        toks = []
+        while True:
+            a = int(amax[b, u])
+            nxt = -1
+            for v in range(nb):
+                if int(parent[b, v]) == u and int(token[b, v]) == a:
+                    nxt = v
+                    break
+            if nxt < 0:
+                break
+            u = nxt
+            path.append(u)
+            toks.append(a)
+        acc_len[b] = len(path) - 1
+        acc_nodes[b, : len(path)] = path
+        acc_tok[b, : len(toks)] = toks
+        acc_tok[b, len(toks)] = int(amax[b, u])
+        bonus[b] = int(amax[b, u])
+    return acc_len, acc_nodes, acc_tok, bonus, amax
