@@ -1,0 +1,462 @@
+#!/usr/bin/env python3
+"""Spec-tree step benchmark: steps/s of topk + tree build + tree attention +
+acceptance on one GB300 (or N replicas, one per GPU), printed as one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Timed region: K CUDA-graph replays of the four library calls, rotating over
+enough input sets that their total exceeds twice the 129 MB L2 (so every step
+reads its inputs from HBM), bracketed by a barrier and device syncs, timed with
+CUDA events on the launching stream; max over ranks.  Per-kernel durations for
+the roofline come from a second pass of eager launches with events between the
+stages, queued behind a GPU sleep so host launch gaps do not count.
+"""
+import os
+
+# the oracle baseline runs single-threaded; pin BLAS before numpy loads
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tree_speculative_decoding_bastion_gb300 import inputs as I  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+DEFAULT_WORKLOAD = "qwen3_8b_b1"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# the oracle on a bounded sample (CPU baseline and the reference arm)
+# ----------------------------------------------------------------------------
+
+
+def oracle_sample_step(inp, target, rows_per_request=64, max_requests=1):
+    """Times the oracle's four stages on the first `max_requests` requests
+    (attention on `rows_per_request` (node, head) rows each) and scales each
+    stage to the whole batch.  Returns (seconds per full step, description)."""
+    import oracle
+    wl = inp.wl
+    r = min(wl.B, max_requests)
+    f32 = lambda a: I.as_f32(a, wl.dtype)
+    t0 = time.perf_counter()
+    x = f32(inp.logits[:r]).reshape(r * wl.K, wl.V)
+    ids, lg, q, lse = oracle.topk_softmax(x, wl.topk)
+    t1 = time.perf_counter()
+    trees = oracle.tree_build(ids.reshape(r, wl.K, -1), lg.reshape(r, wl.K, -1), lse.reshape(r, wl.K),
+                              inp.root_tok[:r], inp.ctx_len[:r], wl.n_min, wl.n_max, inp.C, inp.L_AR)
+    T = oracle.stack_trees(trees)
+    t2 = time.perf_counter()
+    rng = np.random.default_rng(0)
+    rows = []
+    total_rows = 0
+    for b in range(r):
+        nb = int(T["n"][b])
+        total_rows += nb * wl.Hq
+        cand = [(b, i, h) for i in range(nb) for h in range(wl.Hq)]
+        pick = rng.choice(len(cand), size=min(rows_per_request, len(cand)), replace=False)
+        rows += [cand[j] for j in pick]
+
+    class View:
+        def __init__(self, a):
+            self.a = a
+            self.shape = a.shape
+
+        def __getitem__(self, idx):
+            return f32(self.a[idx])
+
+    t3a = time.perf_counter()
+    oracle.tree_attention(View(inp.q), View(inp.k_tree), View(inp.v_tree), View(inp.k_ctx), View(inp.v_ctx),
+                          inp.ctx_len, T["parent"], T["n"], wl.Hkv, inp.scale, block_table=inp.block_table,
+                          page_size=wl.page_size, rows=rows)
+    t3 = time.perf_counter()
+    oracle.accept(View(target[:r]), T["n"], T["parent"], T["token"], wl.K)
+    t4 = time.perf_counter()
+    scale_b = wl.B / r
+    step = scale_b * ((t1 - t0) + (t2 - t1) + (t4 - t3) + (t3 - t3a) * total_rows / max(1, len(rows)))
+    desc = (f"oracle stages 1,2,4 on {r} of {wl.B} requests and attention on {len(rows)} of {total_rows} "
+            f"(node, head) rows, each stage scaled to the full batch")
+    return step, desc
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    wl = I.WORKLOADS[args.workload]
+    inp = I.make_step_inputs(wl, 0)
+    import oracle
+    x = I.as_f32(inp.logits, wl.dtype).reshape(wl.B * wl.K, wl.V)
+    ids, lg, q, lse = oracle.topk_softmax(x, wl.topk)
+    T = oracle.stack_trees(oracle.tree_build(ids.reshape(wl.B, wl.K, -1), lg.reshape(wl.B, wl.K, -1),
+                                             lse.reshape(wl.B, wl.K), inp.root_tok, inp.ctx_len, wl.n_min,
+                                             wl.n_max, inp.C, inp.L_AR))
+    target = I.make_target_logits(inp, T["depth"], T["n"])
+    steps = max(1, min(args.steps, 3))
+    warm = min(args.warmup, 1)
+    for _ in range(warm):
+        oracle_sample_step(inp, target)
+    times = []
+    desc = ""
+    for _ in range(steps):
+        s, desc = oracle_sample_step(inp, target)
+        times.append(s)
+    sec = sum(times)
+    value = steps / sec
+    line = {"impl": "reference", "metric": "spec-tree steps/s", "value": value, "unit": "steps/s",
+            "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": 1000.0 * sec / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(wl, "oracle on host cores"),
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu), "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    p = [x.strip() for x in line.split(",")]
+                    if len(p) >= 10:
+                        rows.append(p)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        busy = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in busy if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        for r in busy:
+            for name, col in (("hw_slowdown", 6), ("hw_thermal_slowdown", 7), ("sw_thermal_slowdown", 8),
+                              ("sw_power_cap", 9)):
+                if r[col].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows), "samples_busy": len(busy)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+
+def config_of(wl, l2):
+    return {"workload": wl.name, "B": wl.B, "K": wl.K, "V": wl.V, "topk": wl.topk, "n_min": wl.n_min,
+            "n_max": wl.n_max, "controller": wl.controller, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": wl.d,
+            "kv_layout": wl.kv_layout, "ctx": wl.L if wl.L_min == 0 else f"U[{wl.L_min},{wl.L}]",
+            "logits": wl.logits, "l2": l2}
+
+
+def stage_bytes(wl, inp, n):
+    """Algorithmic bytes of each stage (every input read once, outputs written once)."""
+    es = 2 if wl.dtype == "bf16" else 4
+    k1 = wl.B * wl.K * wl.V * es
+    kv = 0
+    for b in range(wl.B):
+        L = int(inp.ctx_len[b])
+        nb = int(n[b])
+        kv += 2 * wl.Hkv * wl.d * L * es          # context K and V
+        kv += 2 * nb * wl.Hkv * wl.d * es         # tree K and V
+        kv += 2 * nb * wl.Hq * wl.d * es          # Q in, O out
+    k4 = int(sum(int(n[b]) for b in range(wl.B))) * wl.V * es
+    return {"topk_softmax": k1, "tree_attn": kv, "accept": k4}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from tree_speculative_decoding_bastion_gb300 import binding as bn
+    from tree_speculative_decoding_bastion_gb300 import build
+
+    build.build()
+    torch.cuda.set_device(local_rank)
+    bn.bastion_init(local_rank)
+    wl = I.WORKLOADS[args.workload]
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+
+    def up(x, bf=False):
+        t = torch.from_numpy(np.ascontiguousarray(x.view(np.int16) if bf else x)).cuda()
+        return t.view(torch.bfloat16) if bf else t
+
+    bf = wl.dtype == "bf16"
+
+    # ---- input sets, enough to exceed twice the L2
+    sets = []
+    step = None
+    set_bytes = None
+    n_sets = args.sets
+    r = 0
+    while True:
+        inp = I.make_step_inputs(wl, 1000 * rank + r)
+        s = dict(inp=inp, logits=up(inp.logits, bf), root=up(inp.root_tok), ctx=up(inp.ctx_len),
+                 C=None if inp.C is None else up(inp.C), q=up(inp.q, bf), kt=up(inp.k_tree, bf),
+                 vt=up(inp.v_tree, bf))
+        s["kv"] = bn.KV(up(inp.k_ctx, bf), up(inp.v_ctx, bf),
+                        None if inp.block_table is None else up(inp.block_table))
+        if step is None:
+            step = bn.SpecTreeStep(wl.B, wl.K, wl.V, wl.topk, wl.n_min, wl.n_max, wl.Hq, wl.Hkv, wl.d, s["kv"],
+                                   act_dtype=dt)
+        step.draft(s["logits"], s["root"], s["ctx"], s["C"], inp.L_AR)
+        torch.cuda.synchronize()
+        depth, n = step.depth.cpu().numpy(), step.n.cpu().numpy()
+        s["n"] = n
+        s["target"] = up(I.make_target_logits(inp, depth, n), bf)
+        sets.append(s)
+        if set_bytes is None:
+            set_bytes = sum(t.numel() * t.element_size() for t in
+                            (s["logits"], s["q"], s["kt"], s["vt"], s["kv"].k, s["kv"].v, s["target"]))
+            if n_sets <= 0:
+                n_sets = max(2, min(16, math.ceil(2 * L2_BYTES / set_bytes)))
+        r += 1
+        if r >= n_sets:
+            break
+
+    def args_of(s):
+        return (s["logits"], s["root"], s["ctx"], s["C"], s["inp"].L_AR, s["q"], s["kt"], s["vt"], s["kv"],
+                s["inp"].scale, s["target"])
+
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    # ---- capture one graph per input set
+    graphs = []
+    with torch.cuda.stream(stream):
+        for s in sets:
+            step(*args_of(s))
+    torch.cuda.synchronize()
+    for s in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(*args_of(s))
+        graphs.append(g)
+    torch.cuda.synchronize()
+    launches_per_step = 4
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[i % len(graphs)].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    assert int(step.dev_err.item()) == 0, "device error word set during the benchmark"
+
+    # ---- per-kernel durations: eager stages, events between them
+    names = ("topk_softmax", "tree_build", "tree_attn", "accept")
+    per = {k: [] for k in names}
+    chunk = 16
+    reps = min(max(args.steps, 32), 128)
+    with torch.cuda.stream(stream):
+        for c0 in range(0, reps, chunk):
+            torch.cuda._sleep(int(40e6))   # keeps the GPU busy while the host queues the chunk
+            evs = []
+            for i in range(c0, min(reps, c0 + chunk)):
+                s = sets[i % len(sets)]
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+                ev[0].record(stream)
+                bn.bastion_topk_softmax(s["logits"], wl.topk, step.ids, step.lg, step.q, step.lse, stream=stream)
+                ev[1].record(stream)
+                bn.bastion_tree_build(step.ids, step.lg, step.lse, wl.V, s["root"], s["ctx"], wl.n_min, wl.n_max,
+                                      s["C"], s["inp"].L_AR, step.n, step.parent, step.token, step.depth, step.pos,
+                                      step.rho, step.mask, step.ahat, step.S, step.S_curve, dev_err=step.dev_err,
+                                      stream=stream)
+                ev[2].record(stream)
+                bn.bastion_tree_attn(s["q"], s["kt"], s["vt"], s["kv"], s["ctx"], step.mask, step.n, step.attn_out,
+                                     s["inp"].scale, ws=step.attn_ws, dev_err=step.dev_err, stream=stream)
+                ev[3].record(stream)
+                bn.bastion_accept(s["target"], step.n, step.parent, step.token, wl.K, step.acc_len, step.acc_nodes,
+                                  step.acc_tok, step.bonus, step.acc_ws, argmax_out=step.argmax,
+                                  dev_err=step.dev_err, stream=stream)
+                ev[4].record(stream)
+                evs.append(ev)
+            stream.synchronize()
+            for ev in evs:
+                for j, k in enumerate(names):
+                    per[k].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)   # us
+    clk = clocks.stop()
+    us = {k: statistics.mean(v) for k, v in per.items()}
+    nb = sets[0]["n"]
+    sb = stage_bytes(wl, sets[0]["inp"], nb)
+    dom = max(us, key=us.get)
+    if dom in sb:
+        achieved = sb[dom] / (us[dom] * 1e-6) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None, "bytes_per_launch": sb[dom], "avg_us": us[dom],
+                "peak_kind": f"{peak_kind} (burst copy)"}
+    else:
+        roof = {"kernel": dom, "bound": "alu", "achieved": None, "peak": None, "unit": None, "frac": None,
+                "traffic": None, "avg_us": us[dom]}
+    stages = {k: {"avg_us": us[k],
+                  **({"GB/s": sb[k] / (us[k] * 1e-6) / 1e9, "hbm_frac": sb[k] / (us[k] * 1e-6) / 1e9 / hbm}
+                     if k in sb else {})} for k in names}
+
+    # ---- end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        s = sets[0]
+        host = {k: s[k].cpu().pin_memory() for k in ("logits", "q", "kt", "vt", "target", "root", "ctx")}
+        dev = {k: torch.empty_like(s[k]) for k in host}
+        outs = (step.acc_len, step.acc_tok, step.bonus, step.n)
+        res = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in res)
+        n_e2e = min(max(args.steps, 20), 200)
+        with torch.cuda.stream(stream):
+            for it in range(3 + n_e2e):
+                if it == 3:
+                    stream.synchronize()
+                    t0 = time.perf_counter()
+                for k in host:
+                    dev[k].copy_(host[k], non_blocking=True)
+                step(dev["logits"], dev["root"], dev["ctx"], s["C"], s["inp"].L_AR, dev["q"], dev["kt"], dev["vt"],
+                     s["kv"], s["inp"].scale, dev["target"], stream=stream)
+                for o, h in zip(outs, res):
+                    h.copy_(o, non_blocking=True)
+                stream.synchronize()
+            t1 = time.perf_counter()
+        e2e = {"value": world * n_e2e / (t1 - t0), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h,
+               "note": "per step: H2D of drafter logits, Q, tree K/V, target logits, root/ctx ids from pinned host "
+                       "memory; the four calls; D2H of n, accepted length/tokens, bonus; stream sync. The context "
+                       "KV cache is resident model state"}
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = sets[0]
+        target_np = I.make_target_logits(s["inp"], step.depth.cpu().numpy(), step.n.cpu().numpy())
+        times = []
+        desc = ""
+        t_start = time.perf_counter()
+        while time.perf_counter() - t_start < args.cpu_seconds or not times:
+            t, desc = oracle_sample_step(s["inp"], target_np)
+            times.append(t)
+        cpu = {"value": len(times) / sum(times), "unit": "steps/s", "cores": 1, "kind": "oracle",
+               "sample": desc + f"; {len(times)} samples"}
+
+    if rank == 0:
+        value = world * args.steps / (ms / 1e3)
+        l2 = f"rotating {len(sets)} input sets of {set_bytes / 1e6:.1f} MB (> 2x L2)"
+        line = {"metric": "spec-tree steps/s", "value": value, "unit": "steps/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf else "f32",
+                "data": "synthetic", "config": config_of(wl, l2), "roofline": roof, "stages": stages,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+                "clocks": clk, "tree": {"n": [int(x) for x in nb],
+                                        "ahat": [float(x) for x in step.ahat.cpu().numpy()],
+                                        "acc_len": [int(x) for x in step.acc_len.cpu().numpy()]},
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = enough for 2x L2)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

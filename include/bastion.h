@@ -1,0 +1,219 @@
+/*
+ * bastion.h -- C ABI of the BASTION spec-tree step on one GB300 (sm_103a).
+ *
+ * One decode step of budget-aware tree speculative decoding with
+ * block-diffusion drafting ("Bastion: Budget-Aware Speculative Decoding with
+ * Tree-structured Block Diffusion Drafting", explainer page
+ * gist.science/de/paper/2605.29727, section "Methodik: BASTION") runs as four
+ * calls, in this order, on one CUDA stream:
+ *
+ *   bastion_topk_softmax  per-position marginals q_k and their top-k   (Methodik §1)
+ *   bastion_tree_build    best-first prefix tree + S(N) budget stop      (Methodik §1-§3)
+ *   bastion_tree_attn     tree-masked verification attention            (Problemstellung;
+ *                                                                        "baumgestützte Verifizierung")
+ *   bastion_accept        greedy (temperature 0) acceptance             (Experimentelle Ergebnisse)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every array argument is a DEVICE pointer on the current device, owned and
+ *   allocated by the caller.  The library never allocates, frees or copies
+ *   device memory, never synchronises a stream and keeps no state besides a
+ *   per-device cache of launch properties (filled by bastion_init).
+ * - All work is enqueued on `stream` (NULL = the legacy default stream) and
+ *   returns immediately; results are valid once the stream has reached them.
+ *   The four calls may be captured into a CUDA graph once bastion_init() has
+ *   run for the device outside of any capture.
+ * - Host-detectable problems (NULL pointers, bad sizes, unsupported shapes,
+ *   workspace too small) return an error status synchronously and enqueue
+ *   nothing.  A failed launch returns BASTION_ERR_CUDA.
+ * - Data-dependent problems that only the device can see (a token id >= V,
+ *   n[b] outside [1, n_max], a context length beyond the cache, a page id out of
+ *   range) never fault: the kernel skips the bad access, writes the documented
+ *   fill value and ORs a bit into *dev_err (if dev_err is not NULL).  The
+ *   caller zeroes *dev_err and reads it after its own synchronisation.
+ * - Calls on different streams are independent as long as they do not share
+ *   output buffers or workspaces.
+ * - Workspaces (tree_attn, accept) must be zero-filled once when allocated.
+ *   Every call leaves them zero-filled again in the words that must start at
+ *   zero, so a workspace can be reused without clearing.
+ */
+#ifndef BASTION_H
+#define BASTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *bastion_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  BASTION_OK = 0,
+  BASTION_ERR_INVALID_ARG = 1,  /* NULL pointer, negative or inconsistent size */
+  BASTION_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels handle */
+  BASTION_ERR_WORKSPACE = 3,    /* workspace smaller than the *_workspace_size() */
+  BASTION_ERR_CUDA = 4,         /* a CUDA runtime/driver call or launch failed */
+  BASTION_ERR_NO_DEVICE = 5     /* no usable sm_103 device */
+} bastion_status;
+
+typedef enum { BASTION_F32 = 0, BASTION_BF16 = 1 } bastion_dtype;
+
+/* bits of the device error word */
+#define BASTION_DEVERR_TOKEN 0x1u /* a token id outside [0, V) */
+#define BASTION_DEVERR_N 0x2u     /* n[b] outside [1, n_max] */
+#define BASTION_DEVERR_CTX 0x4u   /* ctx_len[b] < 0 or beyond the KV cache capacity */
+#define BASTION_DEVERR_PAGE 0x8u  /* a block-table page id outside [0, num_pages) */
+#define BASTION_DEVERR_TIMEOUT 0x10u /* a bounded in-kernel wait expired (the call's outputs are invalid) */
+
+/* Limits of this build. */
+#define BASTION_MAX_TOPK 32     /* k of the top-k */
+#define BASTION_MAX_NODES 256   /* n_max, root included */
+#define BASTION_MAX_DEPTH 32    /* K, drafter positions */
+#define BASTION_MAX_VOCAB 262144
+
+/* ABI version of this header (major * 100 + minor). */
+int bastion_abi_version(void);
+
+/* Human-readable name of a status. Never NULL. */
+const char *bastion_status_string(bastion_status s);
+
+/* Explanation of the last error status returned on this host thread
+ * (empty string if none). */
+const char *bastion_last_error(void);
+
+/* Prepare `device` (which must be an sm_103 GPU): caches its SM count and sets
+ * kernel attributes.  Idempotent and thread-safe.  The stage calls run it
+ * implicitly on first use of a device; call it explicitly before capturing the
+ * calls into a CUDA graph. */
+bastion_status bastion_init(int device);
+
+/*
+ * Stage 1 -- per-position marginals and top-k (Methodik §1: the block-diffusion
+ * drafter yields per-position marginals q_k(.) in one forward pass; the tree's
+ * path scores come from drafter logits, "Hauptbeiträge").
+ *
+ * For each of `rows` drafter rows (row r at logits + r * row_stride elements,
+ * V elements, dtype f32 or bf16):
+ *   q(v)   = exp(l_v - m) / sum_u exp(l_u - m)   (softmax over the whole
+ *            vocabulary at temperature 1, m = max logit)
+ *   lse[r] = log sum_u exp(l_u)                  (float64)
+ *   ids[r, 0..k-1] the k tokens of highest logit, ordered by logit descending
+ *            then token id ascending;  lg = their logits (exact, as float),
+ *            q = their probabilities (float, from the float64 lse).
+ * Outputs: ids int32 [rows, k], lg float [rows, k], q float [rows, k],
+ * lse double [rows].  Requires 1 <= k <= min(V, 32), V <= 262144,
+ * row_stride >= V.  Logits must be finite.  No workspace.
+ */
+bastion_status bastion_topk_softmax(const void *logits, bastion_dtype dtype, int rows, int V,
+                                    int64_t row_stride, int k, int32_t *ids, float *lg, float *q,
+                                    double *lse, bastion_stream_t stream);
+
+/*
+ * Stage 2 -- best-first prefix tree with the online budget stop
+ * (Methodik §1 "Pfad-Bewertung": rho(i) = prod_{k=1}^{d(i)} q_k(x_ik);
+ *  §2: A_hat(T) = sum_{i in T} rho(i), best-first repeatedly adds the valid node
+ *  of highest rho; §3: grow until S(N) = A_hat(T_N) * L_AR / C(N) starts to fall).
+ *
+ * Inputs per request b (B requests, K drafter positions, k candidates each):
+ *   ids/lg [B, K, k] and lse [B, K] as produced by stage 1 (row b*K + p is
+ *   position p+1); root_tok [B]; ctx_len [B].
+ * The root is node 0 (token root_tok[b], depth 0, rho 1) and counts in N and in
+ * A_hat.  A node at depth d < K offers the k candidates of position d+1 as
+ * children, rho(child) = rho(parent) * q.  Nodes are added in the order
+ * rho descending, token id ascending, parent index ascending, where rho is
+ * compared through log rho = (fp32 sum of the path's logits, root to leaf) -
+ * (sum of the positions' lse).
+ * Budget:  C == NULL: fixed, n[b] = min(n_max, nodes that exist).
+ *          C != NULL: table C[0..n_max], C[n] = cost of verifying n nodes.
+ *          Nodes are added unconditionally up to n_min; afterwards the next
+ *          node is added only if S(n+1) >= S(n); n[b] is where it stops.
+ * Outputs, rows in insertion (topological) order, unused rows i >= n[b] are
+ * filled with -1 (ints), 0 (rho, mask, S_curve):
+ *   n int32 [B]; parent, token, depth int32 [B, n_max]; pos int32 [B, n_max]
+ *   = ctx_len[b] + depth; rho float [B, n_max]; mask uint64 [B, n_max, W],
+ *   W = ceil(n_max / 64), bit j of row i set iff node j is an ancestor of i or i
+ *   itself; ahat float [B] = A_hat(T_n); S float [B] = S(n) (C == NULL: C = 1);
+ *   S_curve float [B, n_max] (may be NULL): S(i+1) for i < n[b].
+ * Requires 1 <= n_min <= n_max <= 256, 1 <= K <= 32, 1 <= k <= 32, V <= 262144,
+ * L_AR > 0.  Device errors: token id outside [0, V) (BASTION_DEVERR_TOKEN).
+ */
+bastion_status bastion_tree_build(const int32_t *ids, const float *lg, const double *lse, int B,
+                                  int K, int k, int V, const int32_t *root_tok,
+                                  const int32_t *ctx_len, int n_min, int n_max, const float *C,
+                                  float L_AR, int32_t *n, int32_t *parent, int32_t *token,
+                                  int32_t *depth, int32_t *pos, float *rho, uint64_t *mask,
+                                  float *ahat, float *S, float *S_curve, uint32_t *dev_err,
+                                  bastion_stream_t stream);
+
+/* Context KV cache of the verification attention. */
+typedef struct {
+  const void *k;              /* contiguous: [B, Hkv, L_max, d]; paged: [num_pages, Hkv, page_size, d] */
+  const void *v;              /* same layout as k */
+  int64_t L_max;              /* contiguous: context capacity per request; paged: ignored */
+  const int32_t *block_table; /* paged: [B, max_pages] page ids (device); contiguous: NULL */
+  int max_pages;              /* paged: columns of block_table */
+  int num_pages;              /* paged: pages in the pool */
+  int page_size;              /* paged: tokens per page (16) */
+} bastion_kv_cache;
+
+/* Bytes of workspace bastion_tree_attn needs for these sizes. */
+size_t bastion_tree_attn_workspace_size(int B, int n_max, int Hq, int Hkv, int d,
+                                        const bastion_kv_cache *kv);
+
+/*
+ * Stage 3 -- tree-masked verification attention of the tree tokens
+ * (Problemstellung: the target verifies the drafted candidates in one parallel
+ * pass; "Akzeptanzlänge": tree-structured verification).
+ *
+ * For request b, tree node i < n[b] and query head h (KV head h / (Hq/Hkv)):
+ *   out[b,i,h,:] = sum_j softmax_j(q[b,i,h,:] . key_j * scale) value_j
+ * over the keys j = context positions 0..ctx_len[b]-1 of that KV head, followed
+ * by the tree keys k_tree[b,j,kvh,:] of every node j whose bit is set in
+ * mask[b,i,:] (its ancestors and itself).  Q/K/V are already projected and
+ * position-encoded by the caller (tree positions are stage 2's pos).
+ * Layouts: q, out [B, n_max, Hq, d]; k_tree, v_tree [B, n_max, Hkv, d];
+ * mask [B, n_max, ceil(n_max/64)] uint64; n, ctx_len int32 [B].
+ * dtype bf16: tensor-core path (tcgen05, fp32 softmax and accumulation);
+ * dtype f32: exact fp32 path.  out has the input dtype; rows i >= n[b] are not
+ * written.  Requires d in {64, 128}, Hq % Hkv == 0, n_max <= 256, base
+ * pointers 16-byte aligned.  Device errors: BASTION_DEVERR_N, _CTX, _PAGE.
+ */
+bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *v_tree,
+                                 bastion_dtype dtype, int B, int n_max, int Hq, int Hkv, int d,
+                                 float scale, const bastion_kv_cache *kv, const int32_t *ctx_len,
+                                 const uint64_t *mask, const int32_t *n, void *out, void *ws,
+                                 size_t ws_bytes, uint32_t *dev_err, bastion_stream_t stream);
+
+/* Bytes of workspace bastion_accept needs for these sizes. */
+size_t bastion_accept_workspace_size(int B, int n_max);
+
+/*
+ * Stage 4 -- greedy acceptance (Experimentelle Ergebnisse: greedy decoding,
+ * temperature 0; the tree verification keeps the longest valid continuation).
+ *
+ * target: [B, n_max] rows of V logits (row (b,i) at target + (b*n_max+i) *
+ * row_stride elements); only rows i < n[b] are read.
+ *   a_i = argmax_v target[b,i,v] (lowest id on ties).  Walk from the root u = 0:
+ *   while some child c of u (parent[c] == u, c < n[b]) has token[c] == a_u, go
+ *   to it.  Outputs: acc_len int32 [B] accepted draft tokens (0..K);
+ *   acc_nodes int32 [B, K+1] the path root first, -1 padded; acc_tok int32
+ *   [B, K+1] the accepted draft tokens then the bonus token a_u of the last
+ *   node, -1 padded; bonus int32 [B]; argmax_out int32 [B, n_max] (may be
+ *   NULL): a_i for i < n[b], -1 beyond.
+ * Requires V <= 262144 (ids fit the tie-break packing), row_stride >= V,
+ * 1 <= K <= 32, n_max <= 256; target finite.  Invalid n[b]: the request's
+ * outputs are -1 and BASTION_DEVERR_N is set.
+ */
+bastion_status bastion_accept(const void *target, bastion_dtype dtype, int B, int n_max, int V,
+                              int64_t row_stride, int K, const int32_t *n, const int32_t *parent,
+                              const int32_t *token, int32_t *acc_len, int32_t *acc_nodes,
+                              int32_t *acc_tok, int32_t *bonus, int32_t *argmax_out, void *ws,
+                              size_t ws_bytes, uint32_t *dev_err, bastion_stream_t stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* BASTION_H */

@@ -255,6 +255,7 @@ def stack_trees(trees: Sequence[Tree]) -> dict:
         "S": np.array([t.S for t in trees]),
         "S_curve": np.stack([t.S_curve for t in trees]),
         "min_gap": min(t.min_gap for t in trees),
+        "gaps": np.array([t.min_gap for t in trees]),
     }
 
 
@@ -309,7 +310,8 @@ def tree_attention(q, k_tree, v_tree, k_ctx, v_ctx, ctx_len, parent, n, Hkv: int
     if rows is None:
         rows = [(b, i, h) for b in range(B) for i in range(int(n[b])) for h in range(Hq)]
     cache = {}
-    for (b, i, h) in rows:
+    # visit rows grouped by (request, KV head) so each context is read once
+    for (b, i, h) in sorted(rows, key=lambda r: (r[0], r[2] // g, r[1], r[2])):
         kvh = h // g
         if (b, kvh) not in cache:
             cache.clear()

@@ -1,0 +1,115 @@
+"""Test cases for the spec-tree step: seeded inputs, the oracle's results and
+their device copies.
+
+The re-seeding rule: a request is used only if every inexact decision the
+oracle's tree search took for it (cross-depth order of candidates, S(n+1) vs
+S(n)) had a relative rho or S gap of at least 1e-4; otherwise that request's
+drafter logits are redrawn from its seed + 1000.  Exact ties at equal depth are allowed: both sides break them by token
+id, then parent index.
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+
+import oracle
+from tree_speculative_decoding_bastion_gb300 import inputs as I
+
+GAP = 1e-4
+
+
+class Bf16View:
+    """Lazy float32 view of a bf16 bit array (converts only what is indexed)."""
+
+    def __init__(self, bits):
+        self.bits = bits
+        self.shape = bits.shape
+
+    def __getitem__(self, idx):
+        return I.bf16_bits_to_f32(self.bits[idx])
+
+
+def fview(x, dtype):
+    return Bf16View(x) if dtype == "bf16" else x
+
+
+def oracle_draft(inp):
+    """Oracle stages 1-2 on the inputs' drafter logits."""
+    wl = inp.wl
+    x = I.as_f32(inp.logits, wl.dtype).reshape(wl.B * wl.K, wl.V)
+    ids, lg, q, lse = oracle.topk_softmax(x, wl.topk)
+    trees = oracle.tree_build(ids.reshape(wl.B, wl.K, -1), lg.reshape(wl.B, wl.K, -1), lse.reshape(wl.B, wl.K),
+                              inp.root_tok, inp.ctx_len, wl.n_min, wl.n_max, inp.C, inp.L_AR)
+    return dict(ids=ids, lg=lg, q=q, lse=lse, tree=oracle.stack_trees(trees))
+
+
+@functools.lru_cache(maxsize=4)
+def pick(wl: I.Workload, seed: int, with_attention: bool = True):
+    """(inputs, oracle draft) with no near tie in any request.
+
+    A request whose inexact decisions came closer than GAP gets its drafter
+    logits redrawn from seed + 1000 j (the other requests keep theirs)."""
+    req = [seed] * wl.B
+    for _ in range(40):
+        probe = I.make_step_inputs(wl, seed, with_attention=False, req_seeds=tuple(req))
+        o = oracle_draft(probe)
+        bad = [b for b in range(wl.B) if o["tree"]["gaps"][b] < GAP]
+        if not bad:
+            inp = (I.make_step_inputs(wl, seed, with_attention=True, req_seeds=tuple(req))
+                   if with_attention else probe)
+            return inp, o
+        for b in bad:
+            req[b] += 1000
+    raise RuntimeError(f"no seeds without near ties for {wl.name}")
+
+
+def target_for(inp, tree):
+    return I.make_target_logits(inp, tree["depth"], tree["n"])
+
+
+def oracle_attention(inp, tree, rows=None):
+    wl = inp.wl
+    f = lambda a: fview(a, wl.dtype)
+    return oracle.tree_attention(f(inp.q), f(inp.k_tree), f(inp.v_tree), f(inp.k_ctx), f(inp.v_ctx), inp.ctx_len,
+                                 tree["parent"], tree["n"], wl.Hkv, inp.scale, block_table=inp.block_table,
+                                 page_size=wl.page_size, rows=rows)
+
+
+def oracle_accept(inp, tree, target):
+    wl = inp.wl
+    return oracle.accept(fview(target, wl.dtype), tree["n"], tree["parent"], tree["token"], wl.K)
+
+
+# ----------------------------------------------------------------- device side
+
+
+def dev(x, dtype: str = "f32", device="cuda"):
+    """numpy -> torch CUDA tensor; bf16 bit arrays become bfloat16 tensors."""
+    import torch
+    if dtype == "bf16" and x.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+
+def kv_of(inp, device="cuda"):
+    from tree_speculative_decoding_bastion_gb300.binding import KV
+    wl = inp.wl
+    bt = None if inp.block_table is None else dev(inp.block_table, device=device)
+    return KV(dev(inp.k_ctx, wl.dtype, device), dev(inp.v_ctx, wl.dtype, device), bt)
+
+
+def attention_rows(inp, tree, count, seed=0):
+    """A spread of (b, i, h) rows to compare: corners plus random ones."""
+    wl = inp.wl
+    rng = np.random.default_rng(seed)
+    rows = set()
+    for b in range(wl.B):
+        nb = int(tree["n"][b])
+        for i in {0, nb - 1, nb // 2}:
+            for h in {0, wl.Hq - 1}:
+                rows.add((b, i, h))
+    while len(rows) < count:
+        b = int(rng.integers(wl.B))
+        rows.add((b, int(rng.integers(int(tree["n"][b]))), int(rng.integers(wl.Hq))))
+    return sorted(rows)

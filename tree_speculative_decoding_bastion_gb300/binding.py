@@ -1,0 +1,310 @@
+"""Python binding of the C ABI in ``include/bastion.h`` (argument marshalling only).
+
+Every function here takes torch CUDA tensors, checks their dtype/shape/device,
+and passes raw pointers, sizes and the current CUDA stream to
+``libbastion.so``.  All computation happens in the library's kernels; there is
+no CPU or PyTorch fallback.  If the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbastion.so")
+
+BASTION_F32 = 0
+BASTION_BF16 = 1
+DEVERR_TOKEN = 0x1
+DEVERR_N = 0x2
+DEVERR_CTX = 0x4
+DEVERR_PAGE = 0x8
+DEVERR_TIMEOUT = 0x10
+
+_c_int, _c_i64, _c_f, _c_p, _c_sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+
+class BastionError(RuntimeError):
+    pass
+
+
+class KVCache(ctypes.Structure):
+    """Mirror of ``bastion_kv_cache``."""
+    _fields_ = [("k", _c_p), ("v", _c_p), ("L_max", _c_i64), ("block_table", _c_p),
+                ("max_pages", _c_int), ("num_pages", _c_int), ("page_size", _c_int)]
+
+
+_SIGS = {
+    "bastion_abi_version": (_c_int, []),
+    "bastion_status_string": (ctypes.c_char_p, [_c_int]),
+    "bastion_last_error": (ctypes.c_char_p, []),
+    "bastion_init": (_c_int, [_c_int]),
+    "bastion_topk_softmax": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "bastion_tree_build": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_int, _c_int,
+                                    _c_p, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                    _c_p]),
+    "bastion_tree_attn_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(KVCache)]),
+    "bastion_tree_attn": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f,
+                                   ctypes.POINTER(KVCache), _c_p, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "bastion_accept_workspace_size": (_c_sz, [_c_int, _c_int]),
+    "bastion_accept": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p, _c_p]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libbastion.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise BastionError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m tree_speculative_decoding_bastion_gb300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        L = lib()
+        raise BastionError(f"{what}: {L.bastion_status_string(status).decode()} "
+                           f"({L.bastion_last_error().decode()})")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return BASTION_F32
+    if t.dtype == torch.bfloat16:
+        return BASTION_BF16
+    raise BastionError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _need(t: torch.Tensor, dtype, shape, name: str) -> None:
+    if not t.is_cuda:
+        raise BastionError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise BastionError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise BastionError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise BastionError(f"{name} must be contiguous")
+
+
+def bastion_init(device: int = 0) -> None:
+    _check(lib().bastion_init(int(device)), "bastion_init")
+
+
+def bastion_topk_softmax(logits: torch.Tensor, k: int, ids, lg, q, lse, stream=None) -> None:
+    """Stage 1. logits [rows, V] (rows of a [B, K, V] tensor) f32/bf16 with unit
+    element stride; ids int32 [rows, k], lg/q float32 [rows, k], lse float64 [rows]."""
+    if logits.dim() < 2 or logits.stride(-1) != 1:
+        raise BastionError("logits must be [..., V] with contiguous rows")
+    V = logits.shape[-1]
+    flat = logits.reshape(-1, V)
+    rows = flat.shape[0]
+    row_stride = flat.stride(0)
+    for t, dt, name in ((ids, torch.int32, "ids"), (lg, torch.float32, "lg"), (q, torch.float32, "q")):
+        _need(t, dt, None, name)
+        if t.numel() != rows * k:
+            raise BastionError(f"{name} must hold rows*k = {rows * k} elements")
+    _need(lse, torch.float64, None, "lse")
+    if lse.numel() != rows:
+        raise BastionError("lse must hold one value per row")
+    _check(lib().bastion_topk_softmax(_ptr(flat), _dtype_code(logits), rows, V, row_stride, int(k), _ptr(ids),
+                                      _ptr(lg), _ptr(q), _ptr(lse), _stream(stream)), "bastion_topk_softmax")
+
+
+def bastion_tree_build(ids, lg, lse, V: int, root_tok, ctx_len, n_min: int, n_max: int, C: Optional[torch.Tensor],
+                       L_AR: float, n, parent, token, depth, pos, rho, mask, ahat, S, S_curve=None, dev_err=None,
+                       stream=None) -> None:
+    """Stage 2. ids int32 / lg float32 [B, K, k]; lse float64 [B, K]; root_tok, ctx_len int32 [B];
+    C float32 [n_max+1] or None (fixed budget). Outputs as in bastion.h."""
+    B, K, k = ids.shape
+    _need(ids, torch.int32, (B, K, k), "ids")
+    _need(lg, torch.float32, (B, K, k), "lg")
+    _need(lse, torch.float64, (B, K), "lse")
+    _need(root_tok, torch.int32, (B,), "root_tok")
+    _need(ctx_len, torch.int32, (B,), "ctx_len")
+    if C is not None:
+        _need(C, torch.float32, (n_max + 1,), "C")
+    W = (n_max + 63) // 64
+    _need(n, torch.int32, (B,), "n")
+    for t, name in ((parent, "parent"), (token, "token"), (depth, "depth"), (pos, "pos")):
+        _need(t, torch.int32, (B, n_max), name)
+    _need(rho, torch.float32, (B, n_max), "rho")
+    _need(mask, torch.int64, (B, n_max, W), "mask")
+    _need(ahat, torch.float32, (B,), "ahat")
+    _need(S, torch.float32, (B,), "S")
+    if S_curve is not None:
+        _need(S_curve, torch.float32, (B, n_max), "S_curve")
+    if dev_err is not None:
+        _need(dev_err, torch.int32, (1,), "dev_err")
+    _check(lib().bastion_tree_build(_ptr(ids), _ptr(lg), _ptr(lse), B, K, k, int(V), _ptr(root_tok), _ptr(ctx_len),
+                                    int(n_min), int(n_max), _ptr(C), float(L_AR), _ptr(n), _ptr(parent), _ptr(token),
+                                    _ptr(depth), _ptr(pos), _ptr(rho), _ptr(mask), _ptr(ahat), _ptr(S),
+                                    _ptr(S_curve), _ptr(dev_err), _stream(stream)), "bastion_tree_build")
+
+
+@dataclass
+class KV:
+    """Context KV cache: contiguous (k, v [B, Hkv, L_max, d]) or paged
+    (k, v [num_pages, Hkv, page_size, d] + block_table int32 [B, max_pages])."""
+    k: torch.Tensor
+    v: torch.Tensor
+    block_table: Optional[torch.Tensor] = None
+
+    def c_struct(self) -> KVCache:
+        s = KVCache()
+        s.k = self.k.data_ptr()
+        s.v = self.v.data_ptr()
+        if self.block_table is None:
+            s.L_max = self.k.shape[2]
+            s.block_table = None
+            s.max_pages = s.num_pages = s.page_size = 0
+        else:
+            s.L_max = 0
+            s.block_table = self.block_table.data_ptr()
+            s.max_pages = self.block_table.shape[1]
+            s.num_pages = self.k.shape[0]
+            s.page_size = self.k.shape[2]
+        return s
+
+
+def bastion_tree_attn_workspace_size(B: int, n_max: int, Hq: int, Hkv: int, d: int, kv: KV) -> int:
+    s = kv.c_struct()
+    return int(lib().bastion_tree_attn_workspace_size(B, n_max, Hq, Hkv, d, ctypes.byref(s)))
+
+
+def bastion_tree_attn(q, k_tree, v_tree, kv: KV, ctx_len, mask, n, out, scale: float, ws=None, dev_err=None,
+                      stream=None) -> None:
+    """Stage 3. q/out [B, n_max, Hq, d]; k_tree/v_tree [B, n_max, Hkv, d] (same dtype, f32 or bf16)."""
+    B, N, Hq, d = q.shape
+    Hkv = k_tree.shape[2]
+    dt = q.dtype
+    _need(q, dt, None, "q")
+    _need(out, dt, (B, N, Hq, d), "out")
+    _need(k_tree, dt, (B, N, Hkv, d), "k_tree")
+    _need(v_tree, dt, (B, N, Hkv, d), "v_tree")
+    _need(kv.k, dt, None, "kv.k")
+    _need(kv.v, dt, tuple(kv.k.shape), "kv.v")
+    if kv.block_table is not None:
+        _need(kv.block_table, torch.int32, None, "block_table")
+    _need(ctx_len, torch.int32, (B,), "ctx_len")
+    _need(n, torch.int32, (B,), "n")
+    _need(mask, torch.int64, (B, N, (N + 63) // 64), "mask")
+    if ws is not None:
+        _need(ws, torch.uint8, None, "ws")
+    if dev_err is not None:
+        _need(dev_err, torch.int32, (1,), "dev_err")
+    s = kv.c_struct()
+    _check(lib().bastion_tree_attn(_ptr(q), _ptr(k_tree), _ptr(v_tree), _dtype_code(q), B, N, Hq, Hkv, d,
+                                   float(scale), ctypes.byref(s), _ptr(ctx_len), _ptr(mask), _ptr(n), _ptr(out),
+                                   _ptr(ws), 0 if ws is None else ws.numel(), _ptr(dev_err), _stream(stream)),
+           "bastion_tree_attn")
+
+
+def bastion_accept_workspace_size(B: int, n_max: int) -> int:
+    return int(lib().bastion_accept_workspace_size(B, n_max))
+
+
+def bastion_accept(target, n, parent, token, K: int, acc_len, acc_nodes, acc_tok, bonus, ws, argmax_out=None,
+                   dev_err=None, stream=None) -> None:
+    """Stage 4. target [B, n_max, V] f32/bf16 with contiguous rows."""
+    B, N, V = target.shape
+    if target.stride(-1) != 1 or target.stride(0) != N * target.stride(1):
+        raise BastionError("target must be [B, n_max, V] with a uniform row stride")
+    row_stride = target.stride(1)
+    _need(n, torch.int32, (B,), "n")
+    _need(parent, torch.int32, (B, N), "parent")
+    _need(token, torch.int32, (B, N), "token")
+    _need(acc_len, torch.int32, (B,), "acc_len")
+    _need(acc_nodes, torch.int32, (B, K + 1), "acc_nodes")
+    _need(acc_tok, torch.int32, (B, K + 1), "acc_tok")
+    _need(bonus, torch.int32, (B,), "bonus")
+    _need(ws, torch.uint8, None, "ws")
+    if argmax_out is not None:
+        _need(argmax_out, torch.int32, (B, N), "argmax_out")
+    if dev_err is not None:
+        _need(dev_err, torch.int32, (1,), "dev_err")
+    _check(lib().bastion_accept(_ptr(target), _dtype_code(target), B, N, V, row_stride, int(K), _ptr(n),
+                                _ptr(parent), _ptr(token), _ptr(acc_len), _ptr(acc_nodes), _ptr(acc_tok),
+                                _ptr(bonus), _ptr(argmax_out), _ptr(ws), ws.numel(), _ptr(dev_err),
+                                _stream(stream)), "bastion_accept")
+
+
+# --------------------------------------------------------------------------
+# the whole step: buffers + the four calls
+# --------------------------------------------------------------------------
+
+
+class SpecTreeStep:
+    """Owns the output buffers and workspaces of one spec-tree step and runs the
+    four library calls in order on the current stream (no host sync inside)."""
+
+    def __init__(self, B: int, K: int, V: int, topk: int, n_min: int, n_max: int, Hq: int, Hkv: int, d: int,
+                 kv: KV, device="cuda", act_dtype=torch.bfloat16):
+        self.B, self.K, self.V, self.topk = B, K, V, topk
+        self.n_min, self.n_max, self.Hq, self.Hkv, self.d = n_min, n_max, Hq, Hkv, d
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.ids = torch.empty(B, K, topk, **i32)
+        self.lg = torch.empty(B, K, topk, **f32)
+        self.q = torch.empty(B, K, topk, **f32)
+        self.lse = torch.empty(B, K, dtype=torch.float64, device=dev)
+        W = (n_max + 63) // 64
+        self.n = torch.empty(B, **i32)
+        self.parent = torch.empty(B, n_max, **i32)
+        self.token = torch.empty(B, n_max, **i32)
+        self.depth = torch.empty(B, n_max, **i32)
+        self.pos = torch.empty(B, n_max, **i32)
+        self.rho = torch.empty(B, n_max, **f32)
+        self.mask = torch.empty(B, n_max, W, dtype=torch.int64, device=dev)
+        self.ahat = torch.empty(B, **f32)
+        self.S = torch.empty(B, **f32)
+        self.S_curve = torch.empty(B, n_max, **f32)
+        self.attn_out = torch.empty(B, n_max, Hq, d, dtype=act_dtype, device=dev)
+        self.acc_len = torch.empty(B, **i32)
+        self.acc_nodes = torch.empty(B, K + 1, **i32)
+        self.acc_tok = torch.empty(B, K + 1, **i32)
+        self.bonus = torch.empty(B, **i32)
+        self.argmax = torch.empty(B, n_max, **i32)
+        self.dev_err = torch.zeros(1, **i32)
+        self.attn_ws = torch.zeros(max(1, bastion_tree_attn_workspace_size(B, n_max, Hq, Hkv, d, kv)),
+                                   dtype=torch.uint8, device=dev)
+        self.acc_ws = torch.zeros(bastion_accept_workspace_size(B, n_max), dtype=torch.uint8, device=dev)
+
+    def draft(self, logits, root_tok, ctx_len, C, L_AR, stream=None):
+        bastion_topk_softmax(logits, self.topk, self.ids, self.lg, self.q, self.lse, stream=stream)
+        bastion_tree_build(self.ids, self.lg, self.lse, self.V, root_tok, ctx_len, self.n_min, self.n_max, C, L_AR,
+                           self.n, self.parent, self.token, self.depth, self.pos, self.rho, self.mask, self.ahat,
+                           self.S, self.S_curve, dev_err=self.dev_err, stream=stream)
+
+    def verify(self, q, k_tree, v_tree, kv: KV, ctx_len, scale, target, stream=None):
+        bastion_tree_attn(q, k_tree, v_tree, kv, ctx_len, self.mask, self.n, self.attn_out, scale, ws=self.attn_ws,
+                          dev_err=self.dev_err, stream=stream)
+        bastion_accept(target, self.n, self.parent, self.token, self.K, self.acc_len, self.acc_nodes, self.acc_tok,
+                       self.bonus, self.acc_ws, argmax_out=self.argmax, dev_err=self.dev_err, stream=stream)
+
+    def __call__(self, logits, root_tok, ctx_len, C, L_AR, q, k_tree, v_tree, kv: KV, scale, target, stream=None):
+        self.draft(logits, root_tok, ctx_len, C, L_AR, stream=stream)
+        self.verify(q, k_tree, v_tree, kv, ctx_len, scale, target, stream=stream)

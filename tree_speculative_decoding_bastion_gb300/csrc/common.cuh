@@ -1,0 +1,156 @@
+// Device helpers shared by the spec-tree kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/bastion.h"
+
+#define BST_DEV __device__ __forceinline__
+
+namespace bst {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// ---------------------------------------------------------------- element types
+// Element loads: f32 and bf16 logits / activations.  bf16 is kept as raw bits
+// and widened exactly (bits << 16).
+BST_DEV float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
+BST_DEV float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xffff0000u); }
+
+struct F32Tag {
+  using storage = float;
+  static constexpr int kVec = 4;  // elements per 16-byte vector
+};
+struct BF16Tag {
+  using storage = uint16_t;
+  static constexpr int kVec = 8;
+};
+
+// Unpack one 16-byte vector into kVec floats.
+template <class Tag>
+BST_DEV void unpack16(const uint4 &v, float *out);
+template <>
+BST_DEV void unpack16<F32Tag>(const uint4 &v, float *out) {
+  out[0] = __uint_as_float(v.x);
+  out[1] = __uint_as_float(v.y);
+  out[2] = __uint_as_float(v.z);
+  out[3] = __uint_as_float(v.w);
+}
+template <>
+BST_DEV void unpack16<BF16Tag>(const uint4 &v, float *out) {
+  out[0] = bf16_lo(v.x);
+  out[1] = bf16_hi(v.x);
+  out[2] = bf16_lo(v.y);
+  out[3] = bf16_hi(v.y);
+  out[4] = bf16_lo(v.z);
+  out[5] = bf16_hi(v.z);
+  out[6] = bf16_lo(v.w);
+  out[7] = bf16_hi(v.w);
+}
+
+// Element j (0 <= j < kVec, a compile-time constant after unrolling) of a
+// packed 16-byte vector.
+template <class Tag>
+BST_DEV float elem16(const uint4 &v, int j);
+template <>
+BST_DEV float elem16<F32Tag>(const uint4 &v, int j) {
+  const uint32_t w = (j == 0) ? v.x : (j == 1) ? v.y : (j == 2) ? v.z : v.w;
+  return __uint_as_float(w);
+}
+template <>
+BST_DEV float elem16<BF16Tag>(const uint4 &v, int j) {
+  const int q = j >> 1;
+  const uint32_t w = (q == 0) ? v.x : (q == 1) ? v.y : (q == 2) ? v.z : v.w;
+  return (j & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+// Pack kVec floats of a scalar-loaded tail back into the vector form.
+template <class Tag>
+BST_DEV uint4 pack16(const float *f);
+template <>
+BST_DEV uint4 pack16<F32Tag>(const float *f) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+}
+template <>
+BST_DEV uint4 pack16<BF16Tag>(const float *f) {
+  // values came from bf16, so the upper 16 bits carry them exactly
+  auto h = [](float a) { return __float_as_uint(a) >> 16; };
+  return make_uint4(h(f[0]) | (h(f[1]) << 16), h(f[2]) | (h(f[3]) << 16), h(f[4]) | (h(f[5]) << 16),
+                    h(f[6]) | (h(f[7]) << 16));
+}
+
+template <class Tag>
+BST_DEV float load_scalar(const void *base, int64_t idx);
+template <>
+BST_DEV float load_scalar<F32Tag>(const void *base, int64_t idx) {
+  return __ldg(reinterpret_cast<const float *>(base) + idx);
+}
+template <>
+BST_DEV float load_scalar<BF16Tag>(const void *base, int64_t idx) {
+  uint16_t b = __ldg(reinterpret_cast<const unsigned short *>(base) + idx);
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Streaming 16-byte load that does not allocate in L1 (read-once data).
+BST_DEV uint4 ld_stream16(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ---------------------------------------------------------------- ordering keys
+// Order-preserving map float -> uint32 (larger float -> larger uint).  Finite
+// floats never map to 0, which therefore marks "empty".
+BST_DEV uint32_t sortable(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+BST_DEV float unsortable(uint32_t s) {
+  uint32_t u = (s & 0x80000000u) ? (s & 0x7fffffffu) : ~s;
+  return __uint_as_float(u);
+}
+
+// (value, index) candidate ordered by value descending then index ascending.
+struct Cand {
+  float v;
+  int32_t i;
+};
+BST_DEV bool better(float va, int32_t ia, float vb, int32_t ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// 64-bit key: larger is better (value desc, index asc).
+BST_DEV uint64_t pack_vi(float v, int32_t i) {
+  return (static_cast<uint64_t>(sortable(v)) << 32) | static_cast<uint64_t>(0xffffffffu - static_cast<uint32_t>(i));
+}
+BST_DEV float packed_v(uint64_t k) { return unsortable(static_cast<uint32_t>(k >> 32)); }
+BST_DEV int32_t packed_i(uint64_t k) { return static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(k)); }
+
+BST_DEV uint64_t warp_max_u64(uint64_t x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    uint64_t y = __shfl_xor_sync(FULL, x, o);
+    x = y > x ? y : x;
+  }
+  return x;
+}
+BST_DEV float warp_max_f(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(FULL, x, o));
+  return x;
+}
+BST_DEV float warp_sum_f(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(FULL, x, o);
+  return x;
+}
+
+BST_DEV void set_err(uint32_t *err, uint32_t bit) {
+  if (err) atomicOr(err, bit);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace bst

@@ -220,13 +220,19 @@ def latency_table(wl: Workload, seed: int):
     return C, L_AR
 
 
-def make_step_inputs(wl: Workload, seed: int, *, with_attention: bool = True) -> StepInputs:
-    """Draw every input of one step for workload ``wl`` from ``seed``."""
+def make_step_inputs(wl: Workload, seed: int, *, with_attention: bool = True,
+                     req_seeds: Optional[tuple] = None) -> StepInputs:
+    """Draw every input of one step for workload ``wl`` from ``seed``.
+
+    ``req_seeds[b]`` (optional) replaces ``seed`` for request b's drafter
+    logits only, so one request can be redrawn without touching the others.
+    """
     B, K, V = wl.B, wl.K, wl.V
     logits32 = np.empty((B, K, V), dtype=np.float32)
     for b in range(B):
+        sb = seed if req_seeds is None else int(req_seeds[b])
         for k in range(K):
-            logits32[b, k] = _drafter_row(wl, _rng(seed, 1, b, k))
+            logits32[b, k] = _drafter_row(wl, _rng(sb, 1, b, k))
     r = _rng(seed, 2)
     root_tok = r.integers(0, V, size=B).astype(np.int32)
     if wl.L_min > 0:
@@ -267,7 +273,8 @@ def make_step_inputs(wl: Workload, seed: int, *, with_attention: bool = True) ->
         q = k_tree = v_tree = k_ctx = v_ctx = empty
     return StepInputs(wl=wl, seed=seed, logits=store(logits32, wl.dtype), root_tok=root_tok,
                       ctx_len=ctx_len, C=C, L_AR=L_AR, q=q, k_tree=k_tree, v_tree=v_tree,
-                      k_ctx=k_ctx, v_ctx=v_ctx, block_table=block_table)
+                      k_ctx=k_ctx, v_ctx=v_ctx, block_table=block_table,
+                      extra={"req_seeds": None if req_seeds is None else tuple(int(x) for x in req_seeds)})
 
 
 def make_target_logits(inp: StepInputs, depth: np.ndarray, n: np.ndarray) -> np.ndarray:
