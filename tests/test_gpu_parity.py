@@ -132,11 +132,8 @@ def attn_tol(wl):
     return (2e-2, 1e-2) if wl.dtype == "bf16" else (1e-4, 1e-4)
 
 
-@pytest.mark.parametrize("name", list(ALL))
-def test_tree_attention_matches_oracle(name):
-    wl = ALL[name]
-    inp, o = C.pick(wl, 0)
-    tree = o["tree"]
+def _attention_parity(inp, tree, max_rows):
+    wl = inp.wl
     kv = C.kv_of(inp)
     out = torch.full((wl.B, wl.n_max, wl.Hq, wl.d), float("nan"), device="cuda",
                      dtype=torch.bfloat16 if wl.dtype == "bf16" else torch.float32)
@@ -150,7 +147,7 @@ def test_tree_attention_matches_oracle(name):
     assert int(err.item()) == 0
     got = out.float().cpu().numpy()
     total = int(tree["n"].sum()) * wl.Hq
-    rows = None if total <= 4096 else C.attention_rows(inp, tree, 192)
+    rows = None if total <= max_rows else C.attention_rows(inp, tree, max_rows)
     want = C.oracle_attention(inp, tree, rows=rows)
     if rows is None:
         rows = [(b, i, h) for b in range(wl.B) for i in range(int(tree["n"][b])) for h in range(wl.Hq)]
@@ -162,6 +159,18 @@ def test_tree_attention_matches_oracle(name):
     # rows past n[b] are left untouched
     for b in range(wl.B):
         assert np.isnan(got[b, int(tree["n"][b]):]).all()
+    # the split workspace's ticket words are zero again
+    if ws.numel() > 1:
+        units = wl.B * wl.Hkv * ((wl.n_max * wl.g + 127) // 128)
+        assert (ws[: 4 * units].view(torch.int32) == 0).all()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_tree_attention_matches_oracle(name):
+    """Stage 3 alone on the oracle's tree, every (node, head) row compared."""
+    wl = ALL[name]
+    inp, o = C.pick(wl, 0)
+    _attention_parity(inp, o["tree"], max_rows=1 << 30)
 
 
 @pytest.mark.parametrize("name", list(ALL))
@@ -189,11 +198,14 @@ def test_accept_matches_oracle(name):
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_whole_step_matches_oracle(name):
-    """The four calls on device buffers, one stream, no host sync between."""
+def test_attention_and_whole_step_match_oracle(name):
+    """At the workload's full size: stage 3 alone on the oracle's tree (sampled
+    rows), then the four calls on device buffers, one stream, no host sync
+    between, twice in a row on the same workspaces."""
     wl = W[name]
-    inp, o = C.pick(wl, 2)
+    inp, o = C.pick(wl, 0)
     tree = o["tree"]
+    _attention_parity(inp, tree, max_rows=256)
     target = C.target_for(inp, tree)
     kv = C.kv_of(inp)
     step = bn.SpecTreeStep(wl.B, wl.K, wl.V, wl.topk, wl.n_min, wl.n_max, wl.Hq, wl.Hkv, wl.d, kv,

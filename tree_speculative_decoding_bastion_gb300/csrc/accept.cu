@@ -26,7 +26,7 @@ namespace bst {
 
 constexpr int K4_THREADS = 256;
 constexpr int K4_WARPS = K4_THREADS / 32;
-constexpr int K4_U = 8;
+constexpr int K4_U = 16;      // 16-byte loads per thread: 64 KB per CTA in flight
 constexpr int K4_MAXC = 16;
 
 template <class Tag, bool kVecOK>
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(K4_THREADS, 2) accept_kernel(
 #define X(idx) elem16<Tag>(raw[(idx) / VEC], (idx) % VEC)
     float tm = -CUDART_INF_F;
 #pragma unroll
-    for (int j = 0; j < PER; ++j) tm = fmaxf(tm, X(j));
+    for (int u = 0; u < K4_U; ++u) tm = fmaxf(tm, vmax16<Tag>(raw[u]));
     if (tm > bv) {
       // first position (lowest id) holding the tile maximum; elements of a
       // thread are visited in increasing id order
@@ -191,7 +191,11 @@ cudaError_t launch_accept(const void *target, bool bf16, int B, int n_max, int V
                           uint32_t *dev_err, int num_sms, cudaStream_t stream) {
   const int esz = bf16 ? 2 : 4;
   const int rows = B * n_max;
+  // CTAs per row: first enough that each CTA's chunk is one tile (all of its
+  // loads in flight at once), then more while the grid is under two CTAs per SM
+  const int tile = K4_THREADS * K4_U * (16 / esz);
   int C = 1;
+  while (C < K4_MAXC && (V + C - 1) / C > tile) C <<= 1;
   while (C < K4_MAXC && static_cast<int64_t>(rows) * C < 2LL * num_sms && V / (2 * C) >= 4096) C <<= 1;
   const int vec = 16 / esz;
   int chunk = (V + C - 1) / C;

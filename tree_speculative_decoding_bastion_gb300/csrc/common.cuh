@@ -79,6 +79,23 @@ BST_DEV uint4 pack16<BF16Tag>(const float *f) {
                     h(f[6]) | (h(f[7]) << 16));
 }
 
+// Maximum of the kVec elements of a packed 16-byte vector.  bf16 pairs are
+// compared packed (max of bf16 values is exact), then widened once.
+template <class Tag>
+BST_DEV float vmax16(const uint4 &v);
+template <>
+BST_DEV float vmax16<F32Tag>(const uint4 &v) {
+  return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+template <>
+BST_DEV float vmax16<BF16Tag>(const uint4 &v) {
+  uint32_t a, b2;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(b2) : "r"(v.z), "r"(v.w));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(a), "r"(b2));
+  return fmaxf(bf16_lo(a), bf16_hi(a));
+}
+
 template <class Tag>
 BST_DEV float load_scalar(const void *base, int64_t idx);
 template <>

@@ -17,7 +17,8 @@
 //     that provably lies below the tile's k-th largest value (a per-warp sort of
 //     the lane maxima); about 2k candidates survive and are ranked exactly;
 //   * the C partial results (max, sum, sorted top-k) meet in CTA rank 0 through
-//     distributed shared memory, which writes ids, logits, q and lse (float64).
+//     distributed shared memory, which writes ids, logits, q and lse (float64
+//     output; the arithmetic is fp32 with a range-reduced logarithm).
 #include <cooperative_groups.h>
 #include <math_constants.h>
 
@@ -37,11 +38,11 @@ struct K1Smem {
   float wmax[K1_WARPS];
   float wa[K1_WARPS];          // per warp: ceil(k/8)-th largest lane maximum
   float wb[K1_WARPS];          // per warp: k-th largest lane maximum
-  double wsum[K1_WARPS];
+  float wsum[K1_WARPS];
   int cnt;
   int run_n;                   // entries in the running top-k list
   float run_m;                 // running maximum of the chunk
-  double run_s;                // running sum of exp(x - run_m)
+  float run_s;                 // running sum of exp(x - run_m)
   float run_v[BASTION_MAX_TOPK];
   int32_t run_i[BASTION_MAX_TOPK];
   float new_v[BASTION_MAX_TOPK];
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(K1_THREADS, 2) topk_softmax_kernel(
   if (tid == 0) {
     sm.run_n = 0;
     sm.run_m = -CUDART_INF_F;
-    sm.run_s = 0.0;
+    sm.run_s = 0.f;
     sm.cnt = 0;
   }
   __syncthreads();
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(K1_THREADS, 2) topk_softmax_kernel(
       s += sv;
     }
     s = warp_sum_f(s);
-    if (lane == 0) sm.wsum[warp] = static_cast<double>(s);
+    if (lane == 0) sm.wsum[warp] = s;
     __syncthreads();
     const int cnt = sm.cnt;
     if (cnt <= K1_CAP) {
@@ -247,13 +248,13 @@ __global__ void __launch_bounds__(K1_THREADS, 2) topk_softmax_kernel(
       sm.run_i[tid] = sm.new_i[tid];
     }
     if (tid == 0) {
-      double st = 0.0;
+      float st = 0.f;
 #pragma unroll
       for (int w = 0; w < K1_WARPS; ++w) st += sm.wsum[w];
       const float mn = fmaxf(sm.run_m, mt);
-      double acc = 0.0;
-      if (sm.run_m > -CUDART_INF_F) acc += sm.run_s * exp(static_cast<double>(sm.run_m) - mn);
-      if (mt > -CUDART_INF_F) acc += st * exp(static_cast<double>(mt) - mn);
+      float acc = 0.f;
+      if (sm.run_m > -CUDART_INF_F) acc += sm.run_s * expf(sm.run_m - mn);
+      if (mt > -CUDART_INF_F) acc += st * expf(mt - mn);
       sm.run_s = acc;
       sm.run_m = mn;
       sm.cnt = 0;
@@ -267,24 +268,28 @@ __global__ void __launch_bounds__(K1_THREADS, 2) topk_softmax_kernel(
     __shared__ float s_thr;
     __shared__ int s_cnt;
     __shared__ float s_m;
-    __shared__ double s_s;
-    if (tid == 0) {
-      float m = -CUDART_INF_F;
-      float thr = -CUDART_INF_F;
-      for (int c = 0; c < C; ++c) {
-        const K1Smem *o = cluster.map_shared_rank(&sm, c);
-        m = fmaxf(m, o->run_m);
-        if (o->run_n == k) thr = fmaxf(thr, o->run_v[k - 1]);
+    __shared__ float s_s;
+    __shared__ float c_m[K1_MAXC], c_s[K1_MAXC], c_k[K1_MAXC];
+    // one thread per cluster member reads its partial (in parallel), then
+    // warp 0 reduces them
+    if (tid < C) {
+      const K1Smem *o = cluster.map_shared_rank(&sm, tid);
+      c_m[tid] = o->run_m;
+      c_s[tid] = o->run_s;
+      c_k[tid] = (o->run_n == k) ? o->run_v[k - 1] : -CUDART_INF_F;
+    }
+    __syncthreads();
+    if (tid < 32) {
+      const float mc = (lane < C) ? c_m[lane] : -CUDART_INF_F;
+      const float m = warp_max_f(mc);
+      const float sc = warp_sum_f((lane < C && mc > -CUDART_INF_F) ? c_s[lane] * expf(mc - m) : 0.f);
+      const float th = warp_max_f((lane < C) ? c_k[lane] : -CUDART_INF_F);
+      if (lane == 0) {
+        s_m = m;
+        s_s = sc;
+        s_thr = th;
+        s_cnt = 0;
       }
-      double s = 0.0;
-      for (int c = 0; c < C; ++c) {
-        const K1Smem *o = cluster.map_shared_rank(&sm, c);
-        if (o->run_m > -CUDART_INF_F) s += o->run_s * exp(static_cast<double>(o->run_m) - m);
-      }
-      s_m = m;
-      s_s = s;
-      s_thr = thr;
-      s_cnt = 0;
     }
     __syncthreads();
     const float thr = s_thr;
@@ -302,13 +307,19 @@ __global__ void __launch_bounds__(K1_THREADS, 2) topk_softmax_kernel(
     const int M = s_cnt;
     rank_select(sm, M, k);
     __syncthreads();
-    const double L = static_cast<double>(s_m) + log(s_s);
+    // lse = m + ln s with s = 2^e f, f in [0.5, 1): ln s = e ln 2 + ln f keeps
+    // the fp32 logarithm on a small argument (absolute error ~1e-7); only the
+    // final additions run in float64 (this GPU's FP64 pipe is narrow)
+    int e2;
+    const float f = frexpf(s_s, &e2);
+    const double L = static_cast<double>(s_m) + static_cast<double>(e2) * 0.6931471805599453 +
+                     static_cast<double>(logf(f));
     if (tid < k) {
       const int64_t o = static_cast<int64_t>(row) * k + tid;
       const float v = sm.new_v[tid];
       ids[o] = sm.new_i[tid];
       lg[o] = v;
-      q[o] = static_cast<float>(exp(static_cast<double>(v) - L));
+      q[o] = expf(static_cast<float>(static_cast<double>(v) - L));
     }
     if (tid == 0) lse[row] = L;
   }

@@ -85,6 +85,25 @@ struct AttnLayout {
   static constexpr int SMEM = (USED + 1024) > 120 * 1024 ? (USED + 1024) : 120 * 1024;
 };
 
+// Optional phase trace (compiled in with -DBST_TRACE only): %globaltimer
+// stamps at the pipeline's phase boundaries, 32 per CTA, read back with
+// bastion_trace_read().  Normal builds contain none of it.
+#ifdef BST_TRACE
+__device__ unsigned long long g_attn_trace[4096 * 32];
+#define BST_TRACE_AT(ev)                                                                                  \
+  do {                                                                                                  \
+    const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);               \
+    if (cta_ < 4096u && (ev) < 32) g_attn_trace[cta_ * 32u + (ev)] = globaltimer_ns();                 \
+  } while (0)
+extern "C" cudaError_t bastion_trace_read(void *dst, size_t bytes) {
+  return cudaMemcpyFromSymbol(dst, g_attn_trace, bytes);
+}
+#else
+#define BST_TRACE_AT(ev) \
+  do {                   \
+  } while (0)
+#endif
+
 // all threads of the warp agree on the outcome of a bounded wait
 BST_DEV bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
   const bool ok = mbar_wait(bar, parity, abort, ATT_WAIT_NS);
@@ -119,6 +138,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   const int tid = threadIdx.x;
   const int unit = bh * p.mtiles + mtile;
 
+  if (tid == 0) BST_TRACE_AT(0);
   const int nb = p.n[b];
   if (nb < 1 || nb > p.n_max) {
     if (tid == 0 && mtile == 0 && split == 0 && kvh == 0) set_err(p.dev_err, BASTION_DEVERR_N);
@@ -174,6 +194,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
     tc_fence_after();
     const uint32_t tbase = bars->tmem_base;
     const uint32_t tO = tbase + 256;
+    if (tid == 0) BST_TRACE_AT(1);
 
     if (warp == 4) {
       // ------------------------------------------------ TMA producer
@@ -183,6 +204,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_kt);
         tma_prefetch_desc(&tm_vt);
+        BST_TRACE_AT(2);
         mbar_expect_tx(&bars->q_full, LY::Q_BYTES);
 #pragma unroll
         for (int h = 0; h < LY::NH; ++h)
@@ -280,6 +302,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
           }
           any = true;
           mma_commit(&bars->s_full[st]);
+          BST_TRACE_AT(3 + min(j, 7));
           if (j >= 1 && !issue_pv(j - 1)) { run = false; break; }
         }
         if (run) issue_pv(T - 1);
@@ -302,6 +325,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         const int sb = j & 1;
         if (!warp_wait(&bars->s_full[sb], (j >> 1) & 1, abort)) { ok = false; break; }
         tc_fence_after();
+        if (tid == 0) BST_TRACE_AT(11 + min(j, 7));
         uint32_t s[ATT_N];
         tmem_ld32(tbase + lane_off + sb * 128 + 0, s + 0);
         tmem_ld32(tbase + lane_off + sb * 128 + 32, s + 32);
@@ -368,6 +392,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars->p_full[sb]);
+        if (tid == 0) BST_TRACE_AT(19 + min(j, 7));
         m_run = m_new;
       }
       // ---- epilogue: O after the last P V
@@ -375,6 +400,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
       // the drain barrier completes once, after the last P V (and every MMA
       // before it) has finished
       if (ok && !warp_wait(&bars->drain, 0, abort)) ok = false;
+      if (tid == 0) BST_TRACE_AT(27);
       if (ok) {
         tc_fence_after();
 #pragma unroll
@@ -409,6 +435,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
 #pragma unroll
         for (int c = 0; c < D; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
         p.ws_ml[prow] = make_float2(ok ? m_run : -CUDART_INF_F, ok ? l_run : 0.f);
+        if (tid == 0) BST_TRACE_AT(28);
       }
     }
     // all roles done with TMEM
@@ -416,6 +443,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tbase, 512);
+    if (tid == 0) BST_TRACE_AT(31);
     if (*abort && tid == 0) set_err(p.dev_err, BASTION_DEVERR_TIMEOUT);
   } else if (p.splits > 1 && tid < 128) {
     // nothing to attend to in this split: an empty partial
@@ -433,6 +461,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (s_last) {
         __threadfence();
+        if (tid == 0) BST_TRACE_AT(29);
         if (active) {
           const int64_t base = static_cast<int64_t>(unit) * p.splits * ATT_M + r;
           float M = -CUDART_INF_F;
@@ -469,6 +498,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
           }
         }
         if (tid == 0) p.tickets[unit] = 0u;   // ready for the next call
+        if (tid == 0) BST_TRACE_AT(30);
       }
     }
   }

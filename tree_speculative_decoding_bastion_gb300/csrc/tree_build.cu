@@ -17,9 +17,14 @@
 // frontier: node i lives in lane i % 32, register slot i / 32, as a 64-bit key
 // (sortable fp32 log-rho | token | parent) so that one pair of warp max
 // reductions (redux.sync) yields the next node with the exact tie-break
-// (rho desc, token asc, parent asc).  With the controller the pops run in
+// (rho desc, token asc, parent asc).  Node state (path sum, depth, next child
+// rank) lives in shared memory; per insertion every lane computes the two new
+// keys (the parent's next child, the new node's best child) and the owning
+// lanes take them with predicated moves, so the loop never diverges.  With the controller the pops run in
 // chunks of 32; after each chunk the 32 lanes evaluate rho, A_hat and the
 // S(n+1) < S(n) test in parallel and the first drop ends the tree.
+// Arithmetic is fp32 except single float64 additions for the lse prefix
+// (this GPU's FP64 pipe is narrow, so no float64 exp/log/division).
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -27,7 +32,6 @@
 namespace bst {
 
 constexpr int K2_THREADS = 256;
-constexpr int K2_SLOTS = BASTION_MAX_NODES / 32;   // 8 frontier slots per lane
 
 struct K2Smem {
   int32_t ids[BASTION_MAX_DEPTH * BASTION_MAX_TOPK];   // [K][k]
@@ -37,31 +41,25 @@ struct K2Smem {
   float Plo[BASTION_MAX_DEPTH + 1];
   int32_t par[BASTION_MAX_NODES];
   int32_t tok[BASTION_MAX_NODES];
-  int32_t dep[BASTION_MAX_NODES];
+  int32_t dc[BASTION_MAX_NODES];       // depth | (rank of the next child to offer << 8)
   float S32[BASTION_MAX_NODES];        // fp32 logit sum of the path
   float rho[BASTION_MAX_NODES];
-  double ahat[BASTION_MAX_NODES];      // ahat[j] = A_hat after nodes 0..j
+  float ahat[BASTION_MAX_NODES];       // ahat[j] = A_hat after nodes 0..j
   int n_final;
 };
 
-// Frontier candidate of a node: its child of rank c.
-struct Slot {
-  uint32_t hi, lo;   // ordering key; hi == 0 means "no candidate"
-  float S_node;      // path logit sum of the owning node
-  float S_cand;      // path logit sum of the candidate child
-  int32_t dc;        // (node depth) | (child rank << 8)
-};
-
-BST_DEV void make_cand(const K2Smem &sm, int k, int node, float S_node, int d_node, int c, Slot &s) {
-  const float S = S_node + sm.lg[d_node * k + c];             // position d_node + 1
+// Frontier key of "child of rank c of node `node` at depth d_node":
+// high word sortable fp32 log rho (rho desc), low word (0x3FFFF - token) << 8 |
+// (255 - parent) (token asc, then parent asc).  0 means "no candidate".
+BST_DEV uint64_t cand_key(const K2Smem &sm, int k, int node, float S_node, int d_node, int c) {
+  const float S = S_node + sm.lg[d_node * k + c];                    // position d_node + 1
   const float key = (S - sm.Phi[d_node + 1]) - sm.Plo[d_node + 1];   // log rho, fp32
-  s.hi = sortable(key);
-  s.lo = ((0x3FFFFu - static_cast<uint32_t>(sm.ids[d_node * k + c])) << 8) | (255u - static_cast<uint32_t>(node));
-  s.S_node = S_node;
-  s.S_cand = S;
-  s.dc = d_node | (c << 8);
+  const uint32_t lo = ((0x3FFFFu - static_cast<uint32_t>(sm.ids[d_node * k + c])) << 8) |
+                      (255u - static_cast<uint32_t>(node));
+  return (static_cast<uint64_t>(sortable(key)) << 32) | lo;
 }
 
+template <int SLOTS>
 __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
     const int32_t *__restrict__ ids_g, const float *__restrict__ lg_g, const double *__restrict__ lse_g,
     int K, int k, int V, const int32_t *__restrict__ root_tok, const int32_t *__restrict__ ctx_len,
@@ -86,45 +84,47 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
     sm.ids[e] = id;
     sm.lg[e] = lg_g[static_cast<int64_t>(b) * K * k + e];
   }
+  if (tid < 32) {
+    // prefix of the positions' lse (warp scan; K <= 32), kept in float64 and as
+    // an fp32 pair hi + lo for the fp32 keys of the serial loop
+    double P = (tid < K) ? lse_g[static_cast<int64_t>(b) * K + tid] : 0.0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(FULL, P, o);
+      if (tid >= o) P += y;
+    }
+    if (tid < K) {
+      sm.P64[tid + 1] = P;
+      const float hi = static_cast<float>(P);
+      sm.Phi[tid + 1] = hi;
+      sm.Plo[tid + 1] = static_cast<float>(P - static_cast<double>(hi));
+    }
+  }
   if (tid == 0) {
-    double P = 0.0;
     sm.P64[0] = 0.0;
     sm.Phi[0] = 0.f;
     sm.Plo[0] = 0.f;
-    for (int d = 1; d <= K; ++d) {
-      P += lse_g[static_cast<int64_t>(b) * K + d - 1];
-      sm.P64[d] = P;
-      const float hi = static_cast<float>(P);
-      sm.Phi[d] = hi;
-      sm.Plo[d] = static_cast<float>(P - static_cast<double>(hi));
-    }
     int32_t rt = root_tok[b];
     if (rt < 0 || rt >= V) set_err(dev_err, BASTION_DEVERR_TOKEN);
     sm.par[0] = -1;
     sm.tok[0] = rt;
-    sm.dep[0] = 0;
+    sm.dc[0] = 0;
     sm.S32[0] = 0.f;
     sm.rho[0] = 1.f;
-    sm.ahat[0] = 1.0;
+    sm.ahat[0] = 1.f;
     sm.n_final = 1;
   }
   __syncthreads();
 
-  // ---- warp 0: best-first expansion
+  // ---- warp 0: best-first expansion.  Every lane runs the same instruction
+  // stream: both new frontier keys are computed by all lanes, and the two
+  // owning lanes take them with predicated moves.
   if (tid < 32) {
-    Slot slot[K2_SLOTS];
+    uint64_t slot[SLOTS];
 #pragma unroll
-    for (int r = 0; r < K2_SLOTS; ++r) slot[r].hi = 0u, slot[r].lo = 0u, slot[r].S_node = 0.f, slot[r].S_cand = 0.f, slot[r].dc = 0;
-    uint32_t bh = 0u, bl = 0u;
-    float bS = 0.f, bSn = 0.f;
-    int32_t bdc = 0;
-    if (lane == 0 && K >= 1) {
-      make_cand(sm, k, 0, 0.f, 0, 0, slot[0]);
-      bh = slot[0].hi, bl = slot[0].lo, bS = slot[0].S_cand, bSn = slot[0].S_node, bdc = slot[0].dc;
-    }
-    // first-child data of every depth, spread over lanes (lane d holds depth d)
-    const float lg0 = (lane < K) ? sm.lg[lane * k] : 0.f;
-    const int32_t id0 = (lane < K) ? sm.ids[lane * k] : 0;
+    for (int r = 0; r < SLOTS; ++r) slot[r] = 0ull;
+    if (lane == 0) slot[0] = cand_key(sm, k, 0, 0.f, 0, 0);
+    uint64_t best = slot[0];
 
     int n = 1;
     int n_final = -1;
@@ -133,62 +133,40 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
       const int target = controller ? min(n_max, n + 32) : n_max;
       bool exhausted = false;
       while (n < target) {
+        const uint32_t bh = static_cast<uint32_t>(best >> 32);
         const uint32_t mh = __reduce_max_sync(FULL, bh);
         if (mh == 0u) {
           exhausted = true;
           break;
         }
-        const uint32_t ml = __reduce_max_sync(FULL, bh == mh ? bl : 0u);
+        const uint32_t ml = __reduce_max_sync(FULL, bh == mh ? static_cast<uint32_t>(best) : 0u);
         const int p = 255 - static_cast<int>(ml & 0xFFu);
         const int tokn = 0x3FFFF - static_cast<int>(ml >> 8);
-        const int owner = p & 31;
-        const float St = __shfl_sync(FULL, bS, owner);
-        const float Sp = __shfl_sync(FULL, bSn, owner);
-        const int32_t dc = __shfl_sync(FULL, bdc, owner);
-        const int dp = dc & 0xFF;
-        const int c = dc >> 8;
         const int t = n;
+        const int dcp = sm.dc[p];
+        const int dp = dcp & 0xFF;
+        const int c = dcp >> 8;
+        const float Sp = sm.S32[p];
+        const float St = Sp + sm.lg[dp * k + c];   // the same sum the popped key was made from
         const int dt = dp + 1;
-        const float lgf = __shfl_sync(FULL, lg0, dt & 31);
-        const int32_t idf = __shfl_sync(FULL, id0, dt & 31);
+        const uint64_t kP = (c + 1 < k) ? cand_key(sm, k, p, Sp, dp, c + 1) : 0ull;   // p's next child
+        const uint64_t kT = (dt < K) ? cand_key(sm, k, t, St, dt, 0) : 0ull;         // t's best child
         if (lane == 0) {
           sm.par[t] = p;
           sm.tok[t] = tokn;
-          sm.dep[t] = dt;
+          sm.dc[t] = dt;
           sm.S32[t] = St;
+          sm.dc[p] = dcp + 256;
         }
-        if (lane == owner) {
-          // the parent's candidate advances to its next child (or retires)
-          Slot s;
-          s.hi = 0u, s.lo = 0u, s.S_node = Sp, s.S_cand = 0.f, s.dc = 0;
-          if (c + 1 < k) make_cand(sm, k, p, Sp, dp, c + 1, s);
-          const int r = p >> 5;
+        const bool ownP = lane == (p & 31);
+        const bool ownT = lane == (t & 31);
+        const int rp = p >> 5, rt = t >> 5;
+        best = 0ull;
 #pragma unroll
-          for (int j = 0; j < K2_SLOTS; ++j)
-            if (j == r) slot[j] = s;
-          bh = 0u, bl = 0u;
-#pragma unroll
-          for (int j = 0; j < K2_SLOTS; ++j) {
-            if (slot[j].hi > bh || (slot[j].hi == bh && slot[j].lo > bl)) {
-              bh = slot[j].hi, bl = slot[j].lo, bS = slot[j].S_cand, bSn = slot[j].S_node, bdc = slot[j].dc;
-            }
-          }
-        }
-        if (lane == (t & 31) && dt < K) {
-          // the new node offers its best child (rank 0 of position dt + 1)
-          Slot s;
-          const float S = St + lgf;
-          const float key = (S - sm.Phi[dt + 1]) - sm.Plo[dt + 1];
-          s.hi = sortable(key);
-          s.lo = ((0x3FFFFu - static_cast<uint32_t>(idf)) << 8) | (255u - static_cast<uint32_t>(t));
-          s.S_node = St;
-          s.S_cand = S;
-          s.dc = dt;
-          const int r = t >> 5;
-#pragma unroll
-          for (int j = 0; j < K2_SLOTS; ++j)
-            if (j == r) slot[j] = s;
-          if (s.hi > bh || (s.hi == bh && s.lo > bl)) bh = s.hi, bl = s.lo, bS = s.S_cand, bSn = s.S_node, bdc = s.dc;
+        for (int r = 0; r < SLOTS; ++r) {
+          if (ownP && r == rp) slot[r] = kP;
+          if (ownT && r == rt) slot[r] = kT;
+          best = slot[r] > best ? slot[r] : best;
         }
         ++n;
         __syncwarp();
@@ -196,27 +174,25 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
       if (controller) {
         // rho, A_hat and the stop test for the nodes of this chunk
         const int j = chunk_start + lane;
-        double r = 0.0;
+        float r = 0.f;
         if (j < n) {
-          const float key = static_cast<float>(static_cast<double>(sm.S32[j]) - sm.P64[sm.dep[j]]);
-          const float rf = expf(key);
-          sm.rho[j] = rf;
-          r = static_cast<double>(rf);
+          const float key = static_cast<float>(static_cast<double>(sm.S32[j]) - sm.P64[sm.dc[j] & 0xFF]);
+          r = expf(key);
+          sm.rho[j] = r;
         }
         // inclusive prefix sum over the lanes
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(FULL, r, o);
+          const float y = __shfl_up_sync(FULL, r, o);
           if (lane >= o) r += y;
         }
-        const double base = sm.ahat[chunk_start - 1];
-        const double a_next = base + r;                 // A_hat(j + 1)
-        double a_prev = __shfl_up_sync(FULL, a_next, 1);
+        const float base = sm.ahat[chunk_start - 1];
+        const float a_next = base + r;                  // A_hat(j + 1)
+        float a_prev = __shfl_up_sync(FULL, a_next, 1);
         if (lane == 0) a_prev = base;                   // A_hat(j)
         if (j < n) sm.ahat[j] = a_next;
         // tree of size j grows to j + 1 only if S(j + 1) >= S(j)
-        const bool drop = (j < n) && (j >= n_min) &&
-                          (a_next * static_cast<double>(Ctab[j]) < a_prev * static_cast<double>(Ctab[j + 1]));
+        const bool drop = (j < n) && (j >= n_min) && (a_next * Ctab[j] < a_prev * Ctab[j + 1]);
         const unsigned dm = __ballot_sync(FULL, drop);
         if (dm) {
           n_final = chunk_start + (__ffs(dm) - 1);
@@ -237,23 +213,23 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
   // ---- rho and A_hat for a fixed budget (the controller filled them already)
   if (!controller) {
     for (int j = 1 + tid; j < nf; j += K2_THREADS) {
-      const float key = static_cast<float>(static_cast<double>(sm.S32[j]) - sm.P64[sm.dep[j]]);
+      const float key = static_cast<float>(static_cast<double>(sm.S32[j]) - sm.P64[sm.dc[j] & 0xFF]);
       sm.rho[j] = expf(key);
     }
     __syncthreads();
     if (tid < 32) {
       // lane l sums nodes [8l, 8l+8), then an exclusive scan over lanes
-      double part = 0.0;
-      for (int j = 8 * lane; j < min(8 * lane + 8, nf); ++j) part += static_cast<double>(sm.rho[j]);
-      double incl = part;
+      float part = 0.f;
+      for (int j = 8 * lane; j < min(8 * lane + 8, nf); ++j) part += sm.rho[j];
+      float incl = part;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(FULL, incl, o);
+        const float y = __shfl_up_sync(FULL, incl, o);
         if (lane >= o) incl += y;
       }
-      double run = incl - part;
+      float run = incl - part;
       for (int j = 8 * lane; j < min(8 * lane + 8, nf); ++j) {
-        run += static_cast<double>(sm.rho[j]);
+        run += sm.rho[j];
         sm.ahat[j] = run;
       }
     }
@@ -269,12 +245,12 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
     if (i < nf) {
       parent[o] = sm.par[i];
       token[o] = sm.tok[i];
-      depth[o] = sm.dep[i];
-      pos[o] = cl + sm.dep[i];
+      depth[o] = sm.dc[i] & 0xFF;
+      pos[o] = cl + (sm.dc[i] & 0xFF);
       rho_out[o] = sm.rho[i];
       if (S_curve) {
-        const double c = controller ? static_cast<double>(Ctab[i + 1]) : 1.0;
-        S_curve[o] = static_cast<float>(sm.ahat[i] * static_cast<double>(L_AR) / c);
+        const float c = controller ? Ctab[i + 1] : 1.f;
+        S_curve[o] = sm.ahat[i] * L_AR / c;
       }
       unsigned long long m0 = 0, m1 = 0, m2 = 0, m3 = 0;
       int j = i;
@@ -305,10 +281,10 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
   }
   if (tid == 0) {
     n_out[b] = nf;
-    const double a = sm.ahat[nf - 1];
-    const double c = controller ? static_cast<double>(Ctab[nf]) : 1.0;
-    ahat_out[b] = static_cast<float>(a);
-    S_out[b] = static_cast<float>(a * static_cast<double>(L_AR) / c);
+    const float a = sm.ahat[nf - 1];
+    const float c = controller ? Ctab[nf] : 1.f;
+    ahat_out[b] = a;
+    S_out[b] = a * L_AR / c;
   }
 }
 
@@ -317,10 +293,17 @@ cudaError_t launch_tree_build(const int32_t *ids, const float *lg, const double 
                               const float *C, float L_AR, int32_t *n, int32_t *parent, int32_t *token,
                               int32_t *depth, int32_t *pos, float *rho, uint64_t *mask, float *ahat, float *S,
                               float *S_curve, uint32_t *dev_err, cudaStream_t stream) {
-  tree_build_kernel<<<B, K2_THREADS, 0, stream>>>(ids, lg, lse, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR, n,
-                                                  parent, token, depth, pos, rho,
-                                                  reinterpret_cast<unsigned long long *>(mask), ahat, S, S_curve,
-                                                  dev_err);
+  auto *m = reinterpret_cast<unsigned long long *>(mask);
+  // frontier slots per lane: one per 32 nodes of the budget
+  if (n_max <= 64)
+    tree_build_kernel<2><<<B, K2_THREADS, 0, stream>>>(ids, lg, lse, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR,
+                                                       n, parent, token, depth, pos, rho, m, ahat, S, S_curve, dev_err);
+  else if (n_max <= 128)
+    tree_build_kernel<4><<<B, K2_THREADS, 0, stream>>>(ids, lg, lse, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR,
+                                                       n, parent, token, depth, pos, rho, m, ahat, S, S_curve, dev_err);
+  else
+    tree_build_kernel<8><<<B, K2_THREADS, 0, stream>>>(ids, lg, lse, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR,
+                                                       n, parent, token, depth, pos, rho, m, ahat, S, S_curve, dev_err);
   return cudaGetLastError();
 }
 
