@@ -212,6 +212,37 @@ bastion_status bastion_accept(const void *target, bastion_dtype dtype, int B, in
                               int32_t *acc_tok, int32_t *bonus, int32_t *argmax_out, void *ws,
                               size_t ws_bytes, uint32_t *dev_err, bastion_stream_t stream);
 
+/*
+ * bastion_accept_noalloc -- bastion_accept without a workspace argument.
+ *
+ * No counterpart on the pages: this is an interface convenience.  Some callers
+ * cannot allocate device memory when the step runs (an engine that gives all
+ * free GPU memory to its KV cache at start-up and keeps no allocator reachable
+ * from the decode step, or code that must not take the implicit device
+ * synchronisation cudaMalloc / cudaFree can cause).  This call needs no
+ * workspace: its scratch (one ticket word per request, one argmax slot per
+ * tree node) lives in a fixed array of BASTION_ACCEPT_NOALLOC_MAX_BYTES bytes
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  It never calls cudaMalloc, cudaFree or an allocating library
+ * routine.
+ *
+ * Arguments, layouts, results and device-error behaviour are those of
+ * bastion_accept.  Sizes whose scratch (bastion_accept_workspace_size(B, n_max))
+ * exceeds the array return BASTION_ERR_UNSUPPORTED with an explanation in
+ * bastion_last_error().  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call (or bastion_init) before any stream capture.  Each call clears
+ * the ticket words on `stream`, then launches.  All calls share the one array:
+ * calls that overlap on the GPU (different streams, or different host
+ * threads, without ordering between them) race and give wrong results.
+ */
+#define BASTION_ACCEPT_NOALLOC_MAX_BYTES (128u * 1024u)
+bastion_status bastion_accept_noalloc(const void *target, bastion_dtype dtype, int B, int n_max, int V,
+                                      int64_t row_stride, int K, const int32_t *n, const int32_t *parent,
+                                      const int32_t *token, int32_t *acc_len, int32_t *acc_nodes,
+                                      int32_t *acc_tok, int32_t *bonus, int32_t *argmax_out,
+                                      uint32_t *dev_err, bastion_stream_t stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

@@ -53,6 +53,8 @@ _SIGS = {
     "bastion_accept_workspace_size": (_c_sz, [_c_int, _c_int]),
     "bastion_accept": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p,
                                 _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "bastion_accept_noalloc": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_p, _c_p, _c_p,
+                                        _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
 }
 
 _lib = None
@@ -249,6 +251,32 @@ def bastion_accept(target, n, parent, token, K: int, acc_len, acc_nodes, acc_tok
                                 _ptr(parent), _ptr(token), _ptr(acc_len), _ptr(acc_nodes), _ptr(acc_tok),
                                 _ptr(bonus), _ptr(argmax_out), _ptr(ws), ws.numel(), _ptr(dev_err),
                                 _stream(stream)), "bastion_accept")
+
+
+def bastion_accept_noalloc(target, n, parent, token, K: int, acc_len, acc_nodes, acc_tok, bonus, argmax_out=None,
+                           dev_err=None, stream=None) -> None:
+    """Stage 4 without a workspace, for callers that cannot allocate device
+    memory at step time; the scratch is a fixed array inside the library
+    (calls must not overlap on the GPU).  Same arguments as bastion_accept
+    minus ``ws``."""
+    B, N, V = target.shape
+    if target.stride(-1) != 1 or target.stride(0) != N * target.stride(1):
+        raise BastionError("target must be [B, n_max, V] with a uniform row stride")
+    _need(n, torch.int32, (B,), "n")
+    _need(parent, torch.int32, (B, N), "parent")
+    _need(token, torch.int32, (B, N), "token")
+    _need(acc_len, torch.int32, (B,), "acc_len")
+    _need(acc_nodes, torch.int32, (B, K + 1), "acc_nodes")
+    _need(acc_tok, torch.int32, (B, K + 1), "acc_tok")
+    _need(bonus, torch.int32, (B,), "bonus")
+    if argmax_out is not None:
+        _need(argmax_out, torch.int32, (B, N), "argmax_out")
+    if dev_err is not None:
+        _need(dev_err, torch.int32, (1,), "dev_err")
+    _check(lib().bastion_accept_noalloc(_ptr(target), _dtype_code(target), B, N, V, target.stride(1), int(K),
+                                        _ptr(n), _ptr(parent), _ptr(token), _ptr(acc_len), _ptr(acc_nodes),
+                                        _ptr(acc_tok), _ptr(bonus), _ptr(argmax_out), _ptr(dev_err),
+                                        _stream(stream)), "bastion_accept_noalloc")
 
 
 # --------------------------------------------------------------------------

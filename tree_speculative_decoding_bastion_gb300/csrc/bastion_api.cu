@@ -142,6 +142,11 @@ int64_t kv_capacity(const bastion_kv_cache *kv) {
 
 }  // namespace
 
+namespace bst {
+// lets the other translation units of the library record an explanation
+void set_last_error(const std::string &msg) { g_last = msg; }
+}  // namespace bst
+
 extern "C" {
 
 int bastion_abi_version(void) { return 100; }
