@@ -104,11 +104,12 @@ bastion_status bastion_init(int device);
  *            q = their probabilities (float, from the float64 lse).
  * Outputs: ids int32 [rows, k], lg float [rows, k], q float [rows, k],
  * lse double [rows].  Requires 1 <= k <= min(V, 32), V <= 262144,
- * row_stride >= V.  Logits must be finite.  No workspace.
+ * row_stride >= V.  Logits must be finite.  No workspace.  dev_err (nullable)
+ * receives BASTION_DEVERR_TIMEOUT if a staged copy of the row never landed.
  */
 bastion_status bastion_topk_softmax(const void *logits, bastion_dtype dtype, int rows, int V,
                                     int64_t row_stride, int k, int32_t *ids, float *lg, float *q,
-                                    double *lse, bastion_stream_t stream);
+                                    double *lse, uint32_t *dev_err, bastion_stream_t stream);
 
 /*
  * Stage 2 -- best-first prefix tree with the online budget stop
@@ -158,7 +159,8 @@ typedef struct {
   int page_size;              /* paged: tokens per page (16) */
 } bastion_kv_cache;
 
-/* Bytes of workspace bastion_tree_attn needs for these sizes. */
+/* Bytes of workspace bastion_tree_attn needs for these sizes (currently 0:
+ * the KV splits merge inside thread-block clusters; the ws argument is kept). */
 size_t bastion_tree_attn_workspace_size(int B, int n_max, int Hq, int Hkv, int d,
                                         const bastion_kv_cache *kv);
 
@@ -220,8 +222,8 @@ bastion_status bastion_accept(const void *target, bastion_dtype dtype, int B, in
  * free GPU memory to its KV cache at start-up and keeps no allocator reachable
  * from the decode step, or code that must not take the implicit device
  * synchronisation cudaMalloc / cudaFree can cause).  This call needs no
- * workspace: its scratch (one ticket word per request, one argmax slot per
- * tree node) lives in a fixed array of BASTION_ACCEPT_NOALLOC_MAX_BYTES bytes
+ * workspace: its scratch (one ticket word per request, one 8-byte argmax slot
+ * per tree node) lives in a fixed array of BASTION_ACCEPT_NOALLOC_MAX_BYTES bytes
  * inside the library, which every GPU that loads the library holds until the
  * process exits.  It never calls cudaMalloc, cudaFree or an allocating library
  * routine.

@@ -99,17 +99,22 @@ def kv_of(inp, device="cuda"):
     return KV(dev(inp.k_ctx, wl.dtype, device), dev(inp.v_ctx, wl.dtype, device), bt)
 
 
-def attention_rows(inp, tree, count, seed=0):
-    """A spread of (b, i, h) rows to compare: corners plus random ones."""
+def attention_rows(inp, tree, count, seed=0, groups=4):
+    """A spread of (b, i, h) rows to compare: the first and last node of each
+    request and random nodes, drawn from at most `groups` (request, KV head)
+    pairs so that the oracle converts only a few contexts."""
     wl = inp.wl
     rng = np.random.default_rng(seed)
+    pairs = sorted({(b, kvh) for b in range(wl.B) for kvh in range(wl.Hkv)})
+    pick = [pairs[j] for j in sorted(rng.choice(len(pairs), size=min(groups, len(pairs)), replace=False))]
     rows = set()
-    for b in range(wl.B):
+    for (b, kvh) in pick:
         nb = int(tree["n"][b])
+        heads = [kvh * wl.g, kvh * wl.g + wl.g - 1]
         for i in {0, nb - 1, nb // 2}:
-            for h in {0, wl.Hq - 1}:
+            for h in heads:
                 rows.add((b, i, h))
     while len(rows) < count:
-        b = int(rng.integers(wl.B))
-        rows.add((b, int(rng.integers(int(tree["n"][b]))), int(rng.integers(wl.Hq))))
+        b, kvh = pick[int(rng.integers(len(pick)))]
+        rows.add((b, int(rng.integers(int(tree["n"][b]))), kvh * wl.g + int(rng.integers(wl.g))))
     return sorted(rows)

@@ -51,13 +51,13 @@ P = ctypes.c_void_p(16)   # a non-NULL dummy; never dereferenced on these paths
 
 def test_topk_softmax_rejects_bad_arguments(L):
     f = L.bastion_topk_softmax
-    assert f(None, 1, 4, 1024, 1024, 4, P, P, P, P, None) == INVALID
-    assert f(P, 7, 4, 1024, 1024, 4, P, P, P, P, None) == INVALID        # dtype
-    assert f(P, 1, 4, 1024, 1000, 4, P, P, P, P, None) == INVALID        # row_stride < V
-    assert f(P, 1, 0, 1024, 1024, 4, P, P, P, P, None) == INVALID        # rows
-    assert f(P, 1, 4, 1024, 1024, 33, P, P, P, P, None) == UNSUPPORTED   # k > 32
-    assert f(P, 1, 4, 3, 3, 4, P, P, P, P, None) == UNSUPPORTED          # k > V
-    assert f(P, 1, 4, 300000, 300000, 4, P, P, P, P, None) == UNSUPPORTED  # V too large
+    assert f(None, 1, 4, 1024, 1024, 4, P, P, P, P, None, None) == INVALID
+    assert f(P, 7, 4, 1024, 1024, 4, P, P, P, P, None, None) == INVALID        # dtype
+    assert f(P, 1, 4, 1024, 1000, 4, P, P, P, P, None, None) == INVALID        # row_stride < V
+    assert f(P, 1, 0, 1024, 1024, 4, P, P, P, P, None, None) == INVALID        # rows
+    assert f(P, 1, 4, 1024, 1024, 33, P, P, P, P, None, None) == UNSUPPORTED   # k > 32
+    assert f(P, 1, 4, 3, 3, 4, P, P, P, P, None, None) == UNSUPPORTED          # k > V
+    assert f(P, 1, 4, 300000, 300000, 4, P, P, P, P, None, None) == UNSUPPORTED  # V too large
     assert b"topk_softmax" in L.bastion_last_error()
 
 

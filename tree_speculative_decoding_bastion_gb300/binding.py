@@ -43,7 +43,8 @@ _SIGS = {
     "bastion_status_string": (ctypes.c_char_p, [_c_int]),
     "bastion_last_error": (ctypes.c_char_p, []),
     "bastion_init": (_c_int, [_c_int]),
-    "bastion_topk_softmax": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "bastion_topk_softmax": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                      _c_p]),
     "bastion_tree_build": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_int, _c_int,
                                     _c_p, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                                     _c_p]),
@@ -115,7 +116,7 @@ def bastion_init(device: int = 0) -> None:
     _check(lib().bastion_init(int(device)), "bastion_init")
 
 
-def bastion_topk_softmax(logits: torch.Tensor, k: int, ids, lg, q, lse, stream=None) -> None:
+def bastion_topk_softmax(logits: torch.Tensor, k: int, ids, lg, q, lse, dev_err=None, stream=None) -> None:
     """Stage 1. logits [rows, V] (rows of a [B, K, V] tensor) f32/bf16 with unit
     element stride; ids int32 [rows, k], lg/q float32 [rows, k], lse float64 [rows]."""
     if logits.dim() < 2 or logits.stride(-1) != 1:
@@ -131,8 +132,11 @@ def bastion_topk_softmax(logits: torch.Tensor, k: int, ids, lg, q, lse, stream=N
     _need(lse, torch.float64, None, "lse")
     if lse.numel() != rows:
         raise BastionError("lse must hold one value per row")
+    if dev_err is not None:
+        _need(dev_err, torch.int32, (1,), "dev_err")
     _check(lib().bastion_topk_softmax(_ptr(flat), _dtype_code(logits), rows, V, row_stride, int(k), _ptr(ids),
-                                      _ptr(lg), _ptr(q), _ptr(lse), _stream(stream)), "bastion_topk_softmax")
+                                      _ptr(lg), _ptr(q), _ptr(lse), _ptr(dev_err), _stream(stream)),
+           "bastion_topk_softmax")
 
 
 def bastion_tree_build(ids, lg, lse, V: int, root_tok, ctx_len, n_min: int, n_max: int, C: Optional[torch.Tensor],
@@ -322,7 +326,8 @@ class SpecTreeStep:
         self.acc_ws = torch.zeros(bastion_accept_workspace_size(B, n_max), dtype=torch.uint8, device=dev)
 
     def draft(self, logits, root_tok, ctx_len, C, L_AR, stream=None):
-        bastion_topk_softmax(logits, self.topk, self.ids, self.lg, self.q, self.lse, stream=stream)
+        bastion_topk_softmax(logits, self.topk, self.ids, self.lg, self.q, self.lse, dev_err=self.dev_err,
+                             stream=stream)
         bastion_tree_build(self.ids, self.lg, self.lse, self.V, root_tok, ctx_len, self.n_min, self.n_max, C, L_AR,
                            self.n, self.parent, self.token, self.depth, self.pos, self.rho, self.mask, self.ahat,
                            self.S, self.S_curve, dev_err=self.dev_err, stream=stream)

@@ -8,54 +8,59 @@
 // its logits; the accepted path starts at the root and follows the child whose
 // token equals its parent's greedy token.
 //
-// Design: one thread-block cluster per (request, node) row splits the
-// vocabulary into C chunks streamed with 16-byte loads (the HBM-bound part);
-// each thread keeps its first maximum, the CTA and then the cluster (through
-// distributed shared memory) reduce (value desc, id asc) keys.  The row's
-// cluster then takes a ticket on its request; the cluster that completes the
-// request's last row walks the tree (one warp, ballots over the children) and
-// returns the ticket word to zero.
-#include <cooperative_groups.h>
+// Design (HBM-bound vocabulary pass): the C CTAs of a (request, node) row each
+// stage their contiguous chunk of the row into shared memory with bulk
+// asynchronous copies (cp.async.bulk, all of it in flight at once), then find the
+// chunk's first maximum and publish it as a 64-bit key (value desc, id asc)
+// with one atomicMax on the row's slot in the workspace.  Every CTA then takes a
+// ticket on its request; the CTA that completes the request walks the tree
+// (one warp, ballots over the children), and returns the row slots and the
+// ticket to zero for the next call.  No clusters, no inter-CTA waiting.
 #include <math_constants.h>
 
-#include "common.cuh"
-
-namespace cg = cooperative_groups;
+#include "sm100_ptx.cuh"
 
 namespace bst {
 
+#ifdef BST_TRACE
+__device__ unsigned long long g_k4_trace[4096 * 16];
+extern "C" cudaError_t bastion_trace_read_accept(void *dst, size_t bytes) {
+  return cudaMemcpyFromSymbol(dst, g_k4_trace, bytes);
+}
+#endif
+
 constexpr int K4_THREADS = 256;
 constexpr int K4_WARPS = K4_THREADS / 32;
-constexpr int K4_U = 16;      // 16-byte loads per thread: 64 KB per CTA in flight
-constexpr int K4_MAXC = 16;
+constexpr int K4_MAX_CHUNK_BYTES = 48 * 1024;   // shared memory per CTA
+constexpr uint64_t K4_WAIT_NS = 200ull * 1000ull * 1000ull;
 
-template <class Tag, bool kVecOK>
-__global__ void __launch_bounds__(K4_THREADS, 2) accept_kernel(
-    const void *__restrict__ target, int n_max, int V, int64_t row_stride, int K, int chunk,
+// Workspace: [tickets: B x u32, padded to 256 B][row keys: B x n_max x u64]
+__host__ __device__ inline size_t accept_ticket_bytes(int B) { return (static_cast<size_t>(B) * 4 + 255) / 256 * 256; }
+
+template <class Tag, bool kBulk>
+__global__ void __launch_bounds__(K4_THREADS) accept_kernel(
+    const void *__restrict__ target, int n_max, int V, int64_t row_stride, int K, int chunk, int C,
     const int32_t *__restrict__ n_g, const int32_t *__restrict__ parent, const int32_t *__restrict__ token,
     int32_t *__restrict__ acc_len, int32_t *__restrict__ acc_nodes, int32_t *__restrict__ acc_tok,
     int32_t *__restrict__ bonus, int32_t *__restrict__ argmax_out, uint32_t *__restrict__ tickets,
-    int32_t *__restrict__ amax_ws, uint32_t *__restrict__ dev_err) {
+    unsigned long long *__restrict__ rowkey, uint32_t *__restrict__ dev_err) {
   constexpr int VEC = Tag::kVec;
-  constexpr int PER = K4_U * VEC;
-  constexpr int TILE = K4_THREADS * PER;
   using T = typename Tag::storage;
-
-  __shared__ uint64_t s_red[K4_WARPS];
-  __shared__ uint64_t s_best;
+  extern __shared__ __align__(128) uint8_t k4_smem[];
+  __shared__ uint64_t s_bar;
+  __shared__ unsigned long long s_red[K4_WARPS];
   __shared__ int s_last;
 
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = static_cast<int>(cluster.num_blocks());
-  const int crank = static_cast<int>(cluster.block_rank());
+  const int crank = blockIdx.x;
   const int row = blockIdx.y;
   const int b = row / n_max;
   const int i = row - b * n_max;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
+  if (tid == 0) BST_STAMP(g_k4_trace, 0);
   const int nb = n_g[b];
 
-  if (nb < 1 || nb > n_max) {   // uniform for the whole cluster
+  if (nb < 1 || nb > n_max) {   // the whole request is invalid
     if (i == 0 && crank == 0 && tid == 0) {
       set_err(dev_err, BASTION_DEVERR_N);
       acc_len[b] = -1;
@@ -71,85 +76,86 @@ __global__ void __launch_bounds__(K4_THREADS, 2) accept_kernel(
     return;
   }
 
-  // ---- streaming argmax over this CTA's chunk
   const T *rowp = reinterpret_cast<const T *>(target) + static_cast<int64_t>(row) * row_stride;
   const int c0 = crank * chunk;
   const int c1 = min(V, c0 + chunk);
+  const int len = max(0, c1 - c0);
   float bv = -CUDART_INF_F;
   int32_t bi = -1;
-  for (int base = c0; base < c1; base += TILE) {
-    // the tile stays packed in registers (16 bytes per load); padding
-    // positions past the chunk hold -inf
-    uint4 raw[K4_U];
-#pragma unroll
-    for (int u = 0; u < K4_U; ++u) {
-      const int e0 = base + (u * K4_THREADS + tid) * VEC;
-      if (kVecOK && e0 + VEC <= c1) {
-        raw[u] = ld_stream16(rowp + e0);
-      } else {
-        float f[VEC];
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) f[j] = (e0 + j < c1) ? load_scalar<Tag>(rowp, e0 + j) : -CUDART_INF_F;
-        raw[u] = pack16<Tag>(f);
+  if (kBulk) {
+    // ---- stage the chunk into shared memory with bulk copies
+    const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
+    if (tid == 0) {
+      mbar_init(&s_bar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0 && bytes > 0) {
+      mbar_expect_tx(&s_bar, bytes);
+      for (uint32_t off = 0; off < bytes; off += 16384u) {
+        const uint32_t nbytes = min(16384u, bytes - off);
+        bulk_load(k4_smem + off, reinterpret_cast<const uint8_t *>(rowp + c0) + off, nbytes, &s_bar);
       }
     }
-#define X(idx) elem16<Tag>(raw[(idx) / VEC], (idx) % VEC)
-    float tm = -CUDART_INF_F;
+    int no_abort = 0;
+    if (bytes > 0 && !mbar_wait(&s_bar, 0, &no_abort, K4_WAIT_NS)) {
+      if (tid == 0) set_err(dev_err, BASTION_DEVERR_TIMEOUT);
+    } else {
+      // thread t scans 16-byte vectors t, t + 256, ... in increasing order, so
+      // a strict ">" keeps its first maximum
+      const uint4 *v4 = reinterpret_cast<const uint4 *>(k4_smem);
+      const int nvec = len / VEC;
+      for (int v = tid; v < nvec; v += K4_THREADS) {
+        const uint4 x = v4[v];
+        const float m = vmax16<Tag>(x);
+        if (m > bv) {
+          int32_t first = -1;
 #pragma unroll
-    for (int u = 0; u < K4_U; ++u) tm = fmaxf(tm, vmax16<Tag>(raw[u]));
-    if (tm > bv) {
-      // first position (lowest id) holding the tile maximum; elements of a
-      // thread are visited in increasing id order
-      int32_t first = -1;
-#pragma unroll
-      for (int u = K4_U - 1; u >= 0; --u)
-#pragma unroll
-        for (int j = VEC - 1; j >= 0; --j)
-          if (X(u * VEC + j) == tm) first = base + (u * K4_THREADS + tid) * VEC + j;
-      bv = tm;
-      bi = first;
+          for (int j = VEC - 1; j >= 0; --j)
+            if (elem16<Tag>(x, j) == m) first = c0 + v * VEC + j;
+          bv = m;
+          bi = first;
+        }
+      }
+    }
+  } else {
+    // unaligned rows: scalar loads, each thread strides over the chunk
+    for (int e = c0 + tid; e < c1; e += K4_THREADS) {
+      const float x = load_scalar<Tag>(rowp, e);
+      if (x > bv) bv = x, bi = e;
     }
   }
-  uint64_t key = (bi >= 0) ? pack_vi(bv, bi) : 0ull;
+  if (tid == 0) BST_STAMP(g_k4_trace, 1);
+  unsigned long long key = (bi >= 0) ? pack_vi(bv, bi) : 0ull;
   key = warp_max_u64(key);
   if (lane == 0) s_red[tid >> 5] = key;
   __syncthreads();
   if (tid == 0) {
-    uint64_t m = s_red[0];
+    unsigned long long m = s_red[0];
 #pragma unroll
     for (int w = 1; w < K4_WARPS; ++w) m = s_red[w] > m ? s_red[w] : m;
-    s_best = m;
-  }
-  cluster.sync();
-  if (crank == 0 && tid == 0) {
-    uint64_t m = 0;
-    for (int c = 0; c < C; ++c) {
-      const uint64_t o = *cluster.map_shared_rank(&s_best, c);
-      m = o > m ? o : m;
-    }
-    const int32_t a = packed_i(m);
-    amax_ws[row] = a;
-    if (argmax_out) argmax_out[row] = a;
+    if (m) atomicMax(&rowkey[row], m);
     __threadfence();
     const uint32_t t = atomicAdd(&tickets[b], 1u);
-    s_last = (t == static_cast<uint32_t>(nb - 1)) ? 1 : 0;
+    s_last = (t == static_cast<uint32_t>(nb * C - 1)) ? 1 : 0;
+    BST_STAMP(g_k4_trace, 2);
   }
-  cluster.sync();   // remote shared memory no longer needed after this point
-  if (crank != 0) return;
   __syncthreads();
   if (!s_last) return;
 
-  // ---- this cluster finished the request's last row: walk the tree
+  // ---- this CTA completed the request: argmax per node, then walk the tree
+  __threadfence();
+  unsigned long long *rk = rowkey + static_cast<int64_t>(b) * n_max;
+  if (argmax_out)
+    for (int j = tid; j < nb; j += K4_THREADS) argmax_out[static_cast<int64_t>(b) * n_max + j] = packed_i(__ldcg(rk + j));
   if (tid < 32) {
-    __threadfence();
     const int32_t *par = parent + static_cast<int64_t>(b) * n_max;
     const int32_t *tk = token + static_cast<int64_t>(b) * n_max;
-    const int32_t *am = amax_ws + static_cast<int64_t>(b) * n_max;
     int u = 0;
-    int len = 0;
-    int32_t a = __ldcg(am);
+    int len2 = 0;
+    int32_t a = packed_i(__ldcg(rk));
     if (lane == 0) acc_nodes[b * (K + 1)] = 0;
-    while (len < K) {
+    while (len2 < K) {
       int found = -1;
       for (int v0 = 1; v0 < nb; v0 += 32) {
         const int v = v0 + lane;
@@ -161,79 +167,71 @@ __global__ void __launch_bounds__(K4_THREADS, 2) accept_kernel(
         }
       }
       if (found < 0) break;
-      ++len;
+      ++len2;
       if (lane == 0) {
-        acc_nodes[b * (K + 1) + len] = found;
-        acc_tok[b * (K + 1) + len - 1] = a;
+        acc_nodes[b * (K + 1) + len2] = found;
+        acc_tok[b * (K + 1) + len2 - 1] = a;
       }
       u = found;
-      a = __ldcg(am + u);
+      a = packed_i(__ldcg(rk + u));
     }
     if (lane == 0) {
-      acc_len[b] = len;
+      acc_len[b] = len2;
       bonus[b] = a;
-      acc_tok[b * (K + 1) + len] = a;
-      for (int j = len + 1; j <= K; ++j) acc_nodes[b * (K + 1) + j] = -1;
-      for (int j = len + 1; j <= K; ++j) acc_tok[b * (K + 1) + j] = -1;
-      tickets[b] = 0u;   // the workspace word is zero again for the next call
+      acc_tok[b * (K + 1) + len2] = a;
+      for (int j = len2 + 1; j <= K; ++j) acc_nodes[b * (K + 1) + j] = -1;
+      for (int j = len2 + 1; j <= K; ++j) acc_tok[b * (K + 1) + j] = -1;
+      BST_STAMP(g_k4_trace, 3);
     }
   }
+  __syncthreads();
+  // the workspace words are zero again for the next call
+  for (int j = tid; j < nb; j += K4_THREADS) rk[j] = 0ull;
+  if (tid == 0) tickets[b] = 0u;
 }
 
 size_t accept_workspace_size(int B, int n_max) {
-  const size_t t = (static_cast<size_t>(B) * 4 + 255) / 256 * 256;
-  return t + static_cast<size_t>(B) * n_max * 4;
+  return accept_ticket_bytes(B) + static_cast<size_t>(B) * n_max * 8;
 }
 
 cudaError_t launch_accept(const void *target, bool bf16, int B, int n_max, int V, int64_t row_stride, int K,
                           const int32_t *n, const int32_t *parent, const int32_t *token, int32_t *acc_len,
                           int32_t *acc_nodes, int32_t *acc_tok, int32_t *bonus, int32_t *argmax_out, void *ws,
                           uint32_t *dev_err, int num_sms, cudaStream_t stream) {
+  (void)num_sms;
   const int esz = bf16 ? 2 : 4;
   const int rows = B * n_max;
-  // CTAs per row: first enough that each CTA's chunk is one tile (all of its
-  // loads in flight at once), then more while the grid is under two CTAs per SM
-  const int tile = K4_THREADS * K4_U * (16 / esz);
-  int C = 1;
-  while (C < K4_MAXC && (V + C - 1) / C > tile) C <<= 1;
-  while (C < K4_MAXC && static_cast<int64_t>(rows) * C < 2LL * num_sms && V / (2 * C) >= 4096) C <<= 1;
   const int vec = 16 / esz;
+  // CTAs per row: chunks of at most 48 KB, each a multiple of 16 bytes
+  const int max_chunk = K4_MAX_CHUNK_BYTES / esz;
+  int C = (V + max_chunk - 1) / max_chunk;
   int chunk = (V + C - 1) / C;
   chunk = (chunk + vec - 1) / vec * vec;
-  const bool vec_ok = (reinterpret_cast<uintptr_t>(target) % 16 == 0) && ((row_stride * esz) % 16 == 0);
+  C = (V + chunk - 1) / chunk;
+  const bool bulk = (reinterpret_cast<uintptr_t>(target) % 16 == 0) && ((row_stride * esz) % 16 == 0) &&
+                    ((static_cast<int64_t>(V) * esz) % 16 == 0);
   uint32_t *tickets = reinterpret_cast<uint32_t *>(ws);
-  int32_t *amax_ws = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + (static_cast<size_t>(B) * 4 + 255) / 256 * 256);
-
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, rows, 1);
-  cfg.blockDim = dim3(K4_THREADS, 1, 1);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-#define BST_ACCEPT_ARGS target, n_max, V, row_stride, K, chunk, n, parent, token, acc_len, acc_nodes, acc_tok, bonus, argmax_out, tickets, amax_ws, dev_err
+  auto *rowkey = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(ws) + accept_ticket_bytes(B));
+  const dim3 grid(C, rows, 1);
+  const size_t smem = bulk ? static_cast<size_t>(chunk) * esz : 0;
+#define BST_ACCEPT_ARGS target, n_max, V, row_stride, K, chunk, C, n, parent, token, acc_len, acc_nodes, acc_tok, \
+                        bonus, argmax_out, tickets, rowkey, dev_err
   if (bf16) {
-    if (vec_ok) return cudaLaunchKernelEx(&cfg, accept_kernel<BF16Tag, true>, BST_ACCEPT_ARGS);
-    return cudaLaunchKernelEx(&cfg, accept_kernel<BF16Tag, false>, BST_ACCEPT_ARGS);
+    if (bulk) accept_kernel<BF16Tag, true><<<grid, K4_THREADS, smem, stream>>>(BST_ACCEPT_ARGS);
+    else accept_kernel<BF16Tag, false><<<grid, K4_THREADS, 0, stream>>>(BST_ACCEPT_ARGS);
+  } else {
+    if (bulk) accept_kernel<F32Tag, true><<<grid, K4_THREADS, smem, stream>>>(BST_ACCEPT_ARGS);
+    else accept_kernel<F32Tag, false><<<grid, K4_THREADS, 0, stream>>>(BST_ACCEPT_ARGS);
   }
-  if (vec_ok) return cudaLaunchKernelEx(&cfg, accept_kernel<F32Tag, true>, BST_ACCEPT_ARGS);
-  return cudaLaunchKernelEx(&cfg, accept_kernel<F32Tag, false>, BST_ACCEPT_ARGS);
 #undef BST_ACCEPT_ARGS
+  return cudaGetLastError();
 }
 
 cudaError_t prepare_accept() {
   cudaError_t e;
-  e = cudaFuncSetAttribute(accept_kernel<BF16Tag, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  e = cudaFuncSetAttribute(accept_kernel<BF16Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K4_MAX_CHUNK_BYTES);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(accept_kernel<BF16Tag, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(accept_kernel<F32Tag, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(accept_kernel<F32Tag, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaFuncSetAttribute(accept_kernel<F32Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K4_MAX_CHUNK_BYTES);
 }
 
 }  // namespace bst

@@ -84,9 +84,9 @@ extern "C" bastion_status bastion_accept_noalloc(const void *target, bastion_dty
   if (st.err != cudaSuccess || !st.ptr)
     return noalloc_fail(BASTION_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(st.err));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // the ticket words must start at zero; clear them on the caller's stream
-  const size_t ticket_bytes = (static_cast<size_t>(B) * 4 + 255) / 256 * 256;
-  e = cudaMemsetAsync(st.ptr, 0, ticket_bytes, cs);
+  // the ticket words and row slots must start at zero; clear them on the
+  // caller's stream
+  e = cudaMemsetAsync(st.ptr, 0, need, cs);
   if (e != cudaSuccess) return noalloc_fail(BASTION_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
   e = bst::launch_accept(target, dtype == BASTION_BF16, B, n_max, V, row_stride, K, n, parent, token, acc_len,
                          acc_nodes, acc_tok, bonus, argmax_out, st.ptr, dev_err, st.sms, cs);

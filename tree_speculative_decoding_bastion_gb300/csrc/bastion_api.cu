@@ -18,7 +18,8 @@ cudaError_t prepare_topk_softmax();
 cudaError_t prepare_accept();
 cudaError_t prepare_tree_attn();
 cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, int64_t row_stride, int k,
-                                int32_t *ids, float *lg, float *q, double *lse, int num_sms, cudaStream_t stream);
+                                int32_t *ids, float *lg, float *q, double *lse, uint32_t *dev_err, int num_sms,
+                                cudaStream_t stream);
 cudaError_t launch_tree_build(const int32_t *ids, const float *lg, const double *lse, int B, int K, int k, int V,
                               const int32_t *root_tok, const int32_t *ctx_len, int n_min, int n_max, const float *C,
                               float L_AR, int32_t *n, int32_t *parent, int32_t *token, int32_t *depth, int32_t *pos,
@@ -34,7 +35,7 @@ struct AttnPlan {
   int64_t cap;
   size_t ws_bytes, off_o, off_ml;
 };
-AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, int num_sms);
+AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, int num_sms, bool paged);
 cudaError_t launch_tree_attn_tc(const CUtensorMap *maps, const AttnPlan &pl, int B, int n_max, int Hq, int Hkv, int d,
                                 float scale, bool paged, int page_size, int max_pages, int num_pages,
                                 const int32_t *ctx_len, const int32_t *n, const uint64_t *mask,
@@ -179,7 +180,8 @@ bastion_status bastion_init(int device) {
 }
 
 bastion_status bastion_topk_softmax(const void *logits, bastion_dtype dtype, int rows, int V, int64_t row_stride, int k,
-                                    int32_t *ids, float *lg, float *q, double *lse, bastion_stream_t stream) {
+                                    int32_t *ids, float *lg, float *q, double *lse, uint32_t *dev_err,
+                                    bastion_stream_t stream) {
   if (!logits || !ids || !lg || !q || !lse) return fail(BASTION_ERR_INVALID_ARG, "topk_softmax: NULL pointer");
   if (dtype != BASTION_F32 && dtype != BASTION_BF16) return fail(BASTION_ERR_INVALID_ARG, "topk_softmax: bad dtype");
   if (rows < 1 || V < 1 || k < 1 || row_stride < V) return fail(BASTION_ERR_INVALID_ARG, "topk_softmax: bad sizes");
@@ -189,8 +191,8 @@ bastion_status bastion_topk_softmax(const void *logits, bastion_dtype dtype, int
   int sms = 0;
   bastion_status s = current_device(&sms);
   if (s != BASTION_OK) return s;
-  cudaError_t e = bst::launch_topk_softmax(logits, dtype == BASTION_BF16, rows, V, row_stride, k, ids, lg, q, lse, sms,
-                                           reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = bst::launch_topk_softmax(logits, dtype == BASTION_BF16, rows, V, row_stride, k, ids, lg, q, lse,
+                                           dev_err, sms, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "topk_softmax launch");
   return BASTION_OK;
 }
@@ -222,7 +224,7 @@ size_t bastion_tree_attn_workspace_size(int B, int n_max, int Hq, int Hkv, int d
   if (!kv || B < 1 || n_max < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (d != 64 && d != 128)) return 0;
   int sms = 0;
   if (current_device(&sms) != BASTION_OK) return 0;
-  return bst::plan_tree_attn(B, n_max, Hq, Hkv, d, kv_capacity(kv), sms).ws_bytes;
+  return bst::plan_tree_attn(B, n_max, Hq, Hkv, d, kv_capacity(kv), sms, kv->block_table != nullptr).ws_bytes;
 }
 
 bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *v_tree, bastion_dtype dtype, int B,
@@ -266,7 +268,7 @@ bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *
   if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(kv->k) || !aligned16(kv->v) ||
       !aligned16(out))
     return fail(BASTION_ERR_INVALID_ARG, "tree_attn: bf16 tensors must be 16-byte aligned");
-  const bst::AttnPlan pl = bst::plan_tree_attn(B, n_max, Hq, Hkv, d, cap, sms);
+  const bst::AttnPlan pl = bst::plan_tree_attn(B, n_max, Hq, Hkv, d, cap, sms, paged);
   if (pl.ws_bytes > 0 && (!ws || ws_bytes < pl.ws_bytes || !aligned16(ws)))
     return fail(BASTION_ERR_WORKSPACE, "tree_attn: workspace too small (need " + std::to_string(pl.ws_bytes) + " bytes)");
 

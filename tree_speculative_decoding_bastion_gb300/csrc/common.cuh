@@ -170,4 +170,25 @@ BST_DEV void set_err(uint32_t *err, uint32_t bit) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+BST_DEV uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Optional phase trace (compiled in with -DBST_TRACE only): a kernel defines a
+// __device__ buffer of 16 stamps per CTA and records %globaltimer at its phase
+// boundaries.  Normal builds contain none of it.
+#ifdef BST_TRACE
+#define BST_STAMP(buf, ev)                                                                              \
+  do {                                                                                                  \
+    const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);               \
+    if (cta_ < 4096u && (ev) < 16) (buf)[cta_ * 16u + (ev)] = ::bst::now_ns();                          \
+  } while (0)
+#else
+#define BST_STAMP(buf, ev) \
+  do {                     \
+  } while (0)
+#endif
+
 }  // namespace bst

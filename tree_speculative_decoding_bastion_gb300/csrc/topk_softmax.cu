@@ -8,49 +8,63 @@
 // needs only the top-k tokens of each position plus the log-normaliser.
 //
 // Design (HBM-bound vocabulary pass):
-//   * one thread-block cluster per drafter row; the C CTAs of a cluster split
-//     the vocabulary into C contiguous chunks, every byte is read once with
-//     16-byte streaming loads (8 bf16 or 4 fp32 per load, U loads in flight per
-//     thread);
-//   * per tile the chunk lives in registers and is read twice: pass A finds the
-//     maxima, pass B sums exp(x - max) and keeps candidates above a threshold
-//     that provably lies below the tile's k-th largest value (a per-warp sort of
-//     the lane maxima); about 2k candidates survive and are ranked exactly;
-//   * the C partial results (max, sum, sorted top-k) meet in CTA rank 0 through
-//     distributed shared memory, which writes ids, logits, q and lse (float64
-//     output; the arithmetic is fp32 with a range-reduced logarithm).
+//   * one thread-block cluster of C <= 8 CTAs per drafter row; each CTA stages
+//     its contiguous chunk of the row into shared memory with bulk
+//     asynchronous copies (cp.async.bulk: the whole chunk in flight at once);
+//   * two passes over the staged chunk: pass A finds the maxima, pass B sums
+//     exp(x - max) and keeps candidates above a threshold that provably lies
+//     below the chunk's k-th largest value (a per-warp sort of the lane
+//     maxima); about 2k candidates survive and are ranked exactly; a chunk with
+//     more than 1024 candidates (massive ties) takes k exact selection rounds;
+//   * every CTA pushes its partial (max, sum, sorted top-k) into CTA rank 0's
+//     shared memory with remote stores, one cluster barrier follows, and rank 0
+//     merges locally and writes ids, logits, q and lse (float64 output; the
+//     arithmetic is fp32 with a range-reduced logarithm).
 #include <cooperative_groups.h>
 #include <math_constants.h>
 
-#include "common.cuh"
+#include <algorithm>
+
+#include "sm100_ptx.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace bst {
 
+#ifdef BST_TRACE
+__device__ unsigned long long g_k1_trace[4096 * 16];
+extern "C" cudaError_t bastion_trace_read_topk(void *dst, size_t bytes) {
+  return cudaMemcpyFromSymbol(dst, g_k1_trace, bytes);
+}
+#endif
+
 constexpr int K1_THREADS = 256;
 constexpr int K1_WARPS = K1_THREADS / 32;
-constexpr int K1_U = 8;        // 16-byte loads per thread per tile
-constexpr int K1_CAP = 1024;   // candidate buffer per tile
-constexpr int K1_MAXC = 16;    // CTAs per cluster (row)
+constexpr int K1_CAP = 1024;                      // candidate buffer
+constexpr int K1_MAXC = 8;                        // CTAs per cluster (row), portable
+constexpr int K1_CHUNK_BYTES = 48 * 1024;         // preferred staged bytes per CTA
+constexpr int K1_MAX_SMEM = 200 * 1024;           // largest chunk (very long rows)
+constexpr uint64_t K1_WAIT_NS = 200ull * 1000ull * 1000ull;
 
 struct K1Smem {
+  uint64_t bar;
   float wmax[K1_WARPS];
   float wa[K1_WARPS];          // per warp: ceil(k/8)-th largest lane maximum
   float wb[K1_WARPS];          // per warp: k-th largest lane maximum
   float wsum[K1_WARPS];
   int cnt;
-  int run_n;                   // entries in the running top-k list
-  float run_m;                 // running maximum of the chunk
-  float run_s;                 // running sum of exp(x - run_m)
-  float run_v[BASTION_MAX_TOPK];
-  int32_t run_i[BASTION_MAX_TOPK];
+  int nres;
   float new_v[BASTION_MAX_TOPK];
   int32_t new_i[BASTION_MAX_TOPK];
+  unsigned long long red[K1_WARPS];
   float cand_v[K1_CAP + K1_MAXC * BASTION_MAX_TOPK];
   int32_t cand_i[K1_CAP + K1_MAXC * BASTION_MAX_TOPK];
-  uint64_t red[K1_WARPS];
-  float thr;
+  // inbox of CTA rank 0: the partials of every cluster member
+  float in_m[K1_MAXC];
+  float in_s[K1_MAXC];
+  int in_n[K1_MAXC];
+  float in_v[K1_MAXC * BASTION_MAX_TOPK];
+  int32_t in_i[K1_MAXC * BASTION_MAX_TOPK];
 };
 
 // Bitonic sort of one value per lane, descending (lane 0 gets the largest).
@@ -60,12 +74,10 @@ BST_DEV float warp_sort_desc(float v) {
   for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      float o = __shfl_xor_sync(FULL, v, stride);
-      bool up = ((lane & size) == 0);       // this block sorts descending
-      bool lower = ((lane & stride) == 0);  // I hold the lower index of the pair
-      // descending block: lower index keeps the max
-      bool keep_max = (lower == up);
-      v = keep_max ? fmaxf(v, o) : fminf(v, o);
+      const float o = __shfl_xor_sync(FULL, v, stride);
+      const bool up = ((lane & size) == 0);       // this block sorts descending
+      const bool lower = ((lane & stride) == 0);  // I hold the lower index of the pair
+      v = (lower == up) ? fmaxf(v, o) : fminf(v, o);
     }
   }
   return v;
@@ -87,27 +99,51 @@ BST_DEV void rank_select(K1Smem &sm, int M, int k) {
 }
 
 // CTA-wide maximum of a 64-bit key (all threads get it).
-BST_DEV uint64_t cta_max_u64(K1Smem &sm, uint64_t x) {
+BST_DEV unsigned long long cta_max_u64(K1Smem &sm, unsigned long long x) {
   x = warp_max_u64(x);
   const int w = threadIdx.x >> 5;
   __syncthreads();
   if ((threadIdx.x & 31) == 0) sm.red[w] = x;
   __syncthreads();
-  uint64_t r = sm.red[0];
+  unsigned long long r = sm.red[0];
 #pragma unroll
   for (int j = 1; j < K1_WARPS; ++j) r = sm.red[j] > r ? sm.red[j] : r;
   return r;
 }
 
-template <class Tag, bool kVecOK>
-__global__ void __launch_bounds__(K1_THREADS, 2) topk_softmax_kernel(
-    const void *__restrict__ logits, int V, int64_t row_stride, int k, int chunk,
-    int32_t *__restrict__ ids, float *__restrict__ lg, float *__restrict__ q, double *__restrict__ lse) {
-  constexpr int VEC = Tag::kVec;
-  constexpr int PER = K1_U * VEC;             // elements per thread per tile
-  constexpr int TILE = K1_THREADS * PER;
-  using T = typename Tag::storage;
+// 2^x on the special-function unit (the hardware approximation instruction)
+BST_DEV float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
+// Visit every element of the chunk owned by this thread, in increasing order:
+// 16-byte vectors t, t + 256, ... from shared memory (bulk path), or scalars
+// t, t + 256, ... from global memory (unaligned rows).
+template <class Tag, bool kBulk, class F>
+BST_DEV void for_each_elem(const uint8_t *stage, const void *rowp, int c0, int len, F &&f) {
+  constexpr int VEC = Tag::kVec;
+  if (kBulk) {
+    const uint4 *v4 = reinterpret_cast<const uint4 *>(stage);
+    const int nvec = len / VEC;
+    for (int v = threadIdx.x; v < nvec; v += K1_THREADS) {
+      const uint4 x = v4[v];
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) f(elem16<Tag>(x, j), c0 + v * VEC + j);
+    }
+  } else {
+    for (int e = threadIdx.x; e < len; e += K1_THREADS) f(load_scalar<Tag>(rowp, c0 + e), c0 + e);
+  }
+}
+
+template <class Tag, bool kBulk>
+__global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
+    const void *__restrict__ logits, int V, int64_t row_stride, int k, int chunk,
+    int32_t *__restrict__ ids, float *__restrict__ lg, float *__restrict__ q, double *__restrict__ lse,
+    uint32_t *__restrict__ dev_err) {
+  using T = typename Tag::storage;
+  extern __shared__ __align__(128) uint8_t k1_stage[];
   __shared__ K1Smem sm;
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
@@ -118,195 +154,157 @@ __global__ void __launch_bounds__(K1_THREADS, 2) topk_softmax_kernel(
   const int warp = tid >> 5;
   const T *rowp = reinterpret_cast<const T *>(logits) + static_cast<int64_t>(row) * row_stride;
   const int c0 = crank * chunk;
-  const int c1 = min(V, c0 + chunk);
+  const int len = max(0, min(V, c0 + chunk) - c0);
   const int kk = (k + K1_WARPS - 1) / K1_WARPS;
 
+  if (tid == 0) BST_STAMP(g_k1_trace, 0);
   if (tid == 0) {
-    sm.run_n = 0;
-    sm.run_m = -CUDART_INF_F;
-    sm.run_s = 0.f;
     sm.cnt = 0;
+    if (kBulk) {
+      mbar_init(&sm.bar, 1);
+      fence_mbar_init();
+    }
+  }
+  __syncthreads();
+  bool staged = true;
+  if (kBulk) {
+    const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
+    if (tid == 0 && bytes > 0) {
+      mbar_expect_tx(&sm.bar, bytes);
+      for (uint32_t off = 0; off < bytes; off += 16384u)
+        bulk_load(k1_stage + off, reinterpret_cast<const uint8_t *>(rowp + c0) + off, min(16384u, bytes - off), &sm.bar);
+    }
+    int no_abort = 0;
+    if (bytes > 0 && !mbar_wait(&sm.bar, 0, &no_abort, K1_WAIT_NS)) {
+      staged = false;
+      if (tid == 0) set_err(dev_err, BASTION_DEVERR_TIMEOUT);
+    }
+  }
+  const int vlen = staged ? len : 0;   // a copy that never landed counts as empty
+
+  // ---- pass A: maxima and the candidate threshold
+  float tm = -CUDART_INF_F;
+  for_each_elem<Tag, kBulk>(k1_stage, rowp, c0, vlen, [&](float x, int) { tm = fmaxf(tm, x); });
+  const float sorted = warp_sort_desc(tm);
+  const float a_w = __shfl_sync(FULL, sorted, kk - 1);
+  const float b_w = __shfl_sync(FULL, sorted, k - 1);
+  if (lane == 0) {
+    sm.wmax[warp] = sorted;  // lane 0 holds the warp maximum
+    sm.wa[warp] = a_w;
+    sm.wb[warp] = b_w;
+  }
+  __syncthreads();
+  if (tid == 0) BST_STAMP(g_k1_trace, 1);
+  float mt = sm.wmax[0], amin = sm.wa[0], bmax = sm.wb[0];
+#pragma unroll
+  for (int w = 1; w < K1_WARPS; ++w) {
+    mt = fmaxf(mt, sm.wmax[w]);
+    amin = fminf(amin, sm.wa[w]);
+    bmax = fmaxf(bmax, sm.wb[w]);
+  }
+  // Each warp has ceil(k/8) lane maxima >= its a_w, so >= k elements of the
+  // chunk are >= min_w a_w; likewise >= k elements are >= any single b_w.
+  const float thr = fmaxf(amin, bmax);
+
+  // ---- pass B: exp-sum and candidates
+  float s = 0.f;
+  for_each_elem<Tag, kBulk>(k1_stage, rowp, c0, vlen, [&](float x, int idx) {
+    s += ex2f((x - mt) * kLog2e);   // exp(x - m); x - m is exact for bf16 inputs
+    if (x >= thr && x > -CUDART_INF_F) {
+      const int slot = atomicAdd(&sm.cnt, 1);
+      if (slot < K1_CAP) {
+        sm.cand_v[slot] = x;
+        sm.cand_i[slot] = idx;
+      }
+    }
+  });
+  s = warp_sum_f(s);
+  if (lane == 0) sm.wsum[warp] = s;
+  __syncthreads();
+  if (tid == 0) BST_STAMP(g_k1_trace, 2);
+  const int cnt = sm.cnt;
+  if (cnt <= K1_CAP) {
+    rank_select(sm, cnt, k);
+    if (tid == 0) sm.nres = min(k, cnt);
+  } else {
+    // Too many ties at the threshold: exact selection by k rounds of
+    // "best element strictly after the previous pick".
+    float pv = CUDART_INF_F;
+    int32_t pi = -1;
+    int got = 0;
+    for (int r = 0; r < k; ++r) {
+      unsigned long long best = 0;
+      for_each_elem<Tag, kBulk>(k1_stage, rowp, c0, vlen, [&](float x, int idx) {
+        if (x > -CUDART_INF_F && better(pv, pi, x, idx)) {
+          const unsigned long long key = pack_vi(x, idx);
+          best = key > best ? key : best;
+        }
+      });
+      best = cta_max_u64(sm, best);
+      if (best == 0) break;
+      pv = packed_v(best);
+      pi = packed_i(best);
+      if (tid == 0) {
+        sm.new_v[r] = pv;
+        sm.new_i[r] = pi;
+      }
+      ++got;
+    }
+    if (tid == 0) sm.nres = got;
   }
   __syncthreads();
 
-  for (int base = c0; base < c1; base += TILE) {
-    // the tile stays packed in registers (16 bytes per load); padding
-    // positions past the chunk hold -inf
-    uint4 raw[K1_U];
-#pragma unroll
-    for (int u = 0; u < K1_U; ++u) {
-      const int e0 = base + (u * K1_THREADS + tid) * VEC;
-      if (kVecOK && e0 + VEC <= c1) {
-        raw[u] = ld_stream16(rowp + e0);
-      } else {
-        float f[VEC];
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) f[j] = (e0 + j < c1) ? load_scalar<Tag>(rowp, e0 + j) : -CUDART_INF_F;
-        raw[u] = pack16<Tag>(f);
-      }
-    }
-#define X(idx) elem16<Tag>(raw[(idx) / VEC], (idx) % VEC)
-    // ---- pass A: maxima and the candidate threshold
-    float tm = -CUDART_INF_F;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) tm = fmaxf(tm, X(j));
-    const float sorted = warp_sort_desc(tm);
-    const float a_w = __shfl_sync(FULL, sorted, kk - 1);
-    const float b_w = __shfl_sync(FULL, sorted, k - 1);
-    if (lane == 0) {
-      sm.wmax[warp] = sorted;  // lane 0 holds the warp maximum
-      sm.wa[warp] = a_w;
-      sm.wb[warp] = b_w;
-    }
-    __syncthreads();
-    float mt = sm.wmax[0], amin = sm.wa[0], bmax = sm.wb[0];
-#pragma unroll
-    for (int w = 1; w < K1_WARPS; ++w) {
-      mt = fmaxf(mt, sm.wmax[w]);
-      amin = fminf(amin, sm.wa[w]);
-      bmax = fmaxf(bmax, sm.wb[w]);
-    }
-    // Each warp has ceil(k/8) lane maxima >= its a_w, so >= k elements of the
-    // tile are >= min_w a_w; likewise >= k elements are >= any single b_w.
-    // Elements below the running k-th entry cannot enter the list either.
-    float thr = fmaxf(amin, bmax);
-    if (sm.run_n == k) thr = fmaxf(thr, sm.run_v[k - 1]);
-    // ---- pass B: exp-sum and candidates
-    float s = 0.f;
-#pragma unroll
-    for (int u = 0; u < K1_U; ++u) {
-      float sv = 0.f;
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        const float xv = X(u * VEC + j);
-        sv += exp2f((xv - mt) * kLog2e);   // exp(x - m); 0 for padding
-        if (xv >= thr && xv > -CUDART_INF_F) {
-          const int slot = atomicAdd(&sm.cnt, 1);
-          if (slot < K1_CAP) {
-            sm.cand_v[slot] = xv;
-            sm.cand_i[slot] = base + (u * K1_THREADS + tid) * VEC + j;
-          }
-        }
-      }
-      s += sv;
-    }
-    s = warp_sum_f(s);
-    if (lane == 0) sm.wsum[warp] = s;
-    __syncthreads();
-    const int cnt = sm.cnt;
-    if (cnt <= K1_CAP) {
-      // merge the running list into the candidate pool and rank-select
-      const int rn = sm.run_n;
-      for (int j = tid; j < rn; j += K1_THREADS) {
-        sm.cand_v[cnt + j] = sm.run_v[j];
-        sm.cand_i[cnt + j] = sm.run_i[j];
-      }
-      __syncthreads();
-      rank_select(sm, cnt + rn, k);
-      __syncthreads();
-      if (tid == 0) sm.run_n = min(k, cnt + rn);
-    } else {
-      // Too many ties at the threshold: exact selection by k rounds of
-      // "best element strictly after the previous pick" over tile + list.
-      float pv = CUDART_INF_F;
-      int32_t pi = -1;
-      const int rn = sm.run_n;
-      int got = 0;
-      for (int r = 0; r < k; ++r) {
-        uint64_t best = 0;
-#pragma unroll
-        for (int u = 0; u < K1_U; ++u) {
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) {
-            const float xv = X(u * VEC + j);
-            const int32_t xi = base + (u * K1_THREADS + tid) * VEC + j;
-            if (xv > -CUDART_INF_F && better(pv, pi, xv, xi)) {
-              const uint64_t key = pack_vi(xv, xi);
-              best = key > best ? key : best;
-            }
-          }
-        }
-        if (tid < rn && better(pv, pi, sm.run_v[tid], sm.run_i[tid])) {
-          const uint64_t key = pack_vi(sm.run_v[tid], sm.run_i[tid]);
-          best = key > best ? key : best;
-        }
-        best = cta_max_u64(sm, best);
-        if (best == 0) break;
-        pv = packed_v(best);
-        pi = packed_i(best);
-        if (tid == 0) {
-          sm.new_v[r] = pv;
-          sm.new_i[r] = pi;
-        }
-        ++got;
-      }
-      __syncthreads();
-      if (tid == 0) sm.run_n = got;
-    }
-    if (tid < k) {
-      sm.run_v[tid] = sm.new_v[tid];
-      sm.run_i[tid] = sm.new_i[tid];
-    }
-    if (tid == 0) {
-      float st = 0.f;
-#pragma unroll
-      for (int w = 0; w < K1_WARPS; ++w) st += sm.wsum[w];
-      const float mn = fmaxf(sm.run_m, mt);
-      float acc = 0.f;
-      if (sm.run_m > -CUDART_INF_F) acc += sm.run_s * expf(sm.run_m - mn);
-      if (mt > -CUDART_INF_F) acc += st * expf(mt - mn);
-      sm.run_s = acc;
-      sm.run_m = mn;
-      sm.cnt = 0;
-    }
-    __syncthreads();
+  // ---- push this CTA's partial into rank 0's inbox, then one cluster barrier
+  K1Smem *r0 = cluster.map_shared_rank(&sm, 0);
+  const int nres = sm.nres;
+  if (tid < nres) {
+    r0->in_v[crank * BASTION_MAX_TOPK + tid] = sm.new_v[tid];
+    r0->in_i[crank * BASTION_MAX_TOPK + tid] = sm.new_i[tid];
   }
-
-  // ---- cluster merge in CTA rank 0 over distributed shared memory
+  if (tid == 0) {
+    float st = 0.f;
+#pragma unroll
+    for (int w = 0; w < K1_WARPS; ++w) st += sm.wsum[w];
+    r0->in_m[crank] = mt;
+    r0->in_s[crank] = st;
+    r0->in_n[crank] = nres;
+    BST_STAMP(g_k1_trace, 3);
+  }
   cluster.sync();
-  if (crank == 0) {
-    __shared__ float s_thr;
-    __shared__ int s_cnt;
-    __shared__ float s_m;
-    __shared__ float s_s;
-    __shared__ float c_m[K1_MAXC], c_s[K1_MAXC], c_k[K1_MAXC];
-    // one thread per cluster member reads its partial (in parallel), then
-    // warp 0 reduces them
-    if (tid < C) {
-      const K1Smem *o = cluster.map_shared_rank(&sm, tid);
-      c_m[tid] = o->run_m;
-      c_s[tid] = o->run_s;
-      c_k[tid] = (o->run_n == k) ? o->run_v[k - 1] : -CUDART_INF_F;
+  if (tid == 0) BST_STAMP(g_k1_trace, 4);
+  if (crank != 0) return;
+
+  // ---- rank 0: merge the C partials from its own shared memory
+  __shared__ float s_thr, s_m, s_s;
+  __shared__ int s_cnt;
+  if (tid < 32) {
+    const float mc = (lane < C) ? sm.in_m[lane] : -CUDART_INF_F;
+    const float m = warp_max_f(mc);
+    const float sc = warp_sum_f((lane < C && mc > -CUDART_INF_F) ? sm.in_s[lane] * expf(mc - m) : 0.f);
+    // every partial list holding k entries bounds the k-th best from below
+    const float th = warp_max_f((lane < C && sm.in_n[lane] == k) ? sm.in_v[lane * BASTION_MAX_TOPK + k - 1]
+                                                                 : -CUDART_INF_F);
+    if (lane == 0) {
+      s_m = m;
+      s_s = sc;
+      s_thr = th;
+      s_cnt = 0;
     }
-    __syncthreads();
-    if (tid < 32) {
-      const float mc = (lane < C) ? c_m[lane] : -CUDART_INF_F;
-      const float m = warp_max_f(mc);
-      const float sc = warp_sum_f((lane < C && mc > -CUDART_INF_F) ? c_s[lane] * expf(mc - m) : 0.f);
-      const float th = warp_max_f((lane < C) ? c_k[lane] : -CUDART_INF_F);
-      if (lane == 0) {
-        s_m = m;
-        s_s = sc;
-        s_thr = th;
-        s_cnt = 0;
-      }
+  }
+  __syncthreads();
+  const float thr2 = s_thr;
+  for (int e = tid; e < C * BASTION_MAX_TOPK; e += K1_THREADS) {
+    const int c = e / BASTION_MAX_TOPK, j = e % BASTION_MAX_TOPK;
+    if (j < sm.in_n[c] && sm.in_v[e] >= thr2) {
+      const int slot = atomicAdd(&s_cnt, 1);
+      sm.cand_v[slot] = sm.in_v[e];
+      sm.cand_i[slot] = sm.in_i[e];
     }
-    __syncthreads();
-    const float thr = s_thr;
-    // gather every list entry >= thr (at least k of them exist)
-    for (int e = tid; e < C * k; e += K1_THREADS) {
-      const int c = e / k, j = e % k;
-      const K1Smem *o = cluster.map_shared_rank(&sm, c);
-      if (j < o->run_n && o->run_v[j] >= thr) {
-        const int slot = atomicAdd(&s_cnt, 1);
-        sm.cand_v[slot] = o->run_v[j];
-        sm.cand_i[slot] = o->run_i[j];
-      }
-    }
-    __syncthreads();
-    const int M = s_cnt;
-    rank_select(sm, M, k);
-    __syncthreads();
+  }
+  __syncthreads();
+  rank_select(sm, s_cnt, k);
+  __syncthreads();
+  if (tid < k) {
     // lse = m + ln s with s = 2^e f, f in [0.5, 1): ln s = e ln 2 + ln f keeps
     // the fp32 logarithm on a small argument (absolute error ~1e-7); only the
     // final additions run in float64 (this GPU's FP64 pipe is narrow)
@@ -314,36 +312,38 @@ __global__ void __launch_bounds__(K1_THREADS, 2) topk_softmax_kernel(
     const float f = frexpf(s_s, &e2);
     const double L = static_cast<double>(s_m) + static_cast<double>(e2) * 0.6931471805599453 +
                      static_cast<double>(logf(f));
-    if (tid < k) {
-      const int64_t o = static_cast<int64_t>(row) * k + tid;
-      const float v = sm.new_v[tid];
-      ids[o] = sm.new_i[tid];
-      lg[o] = v;
-      q[o] = expf(static_cast<float>(static_cast<double>(v) - L));
-    }
+    const int64_t o = static_cast<int64_t>(row) * k + tid;
+    const float v = sm.new_v[tid];
+    ids[o] = sm.new_i[tid];
+    lg[o] = v;
+    q[o] = expf(static_cast<float>(static_cast<double>(v) - L));
     if (tid == 0) lse[row] = L;
   }
-  cluster.sync();   // keep every CTA's shared memory alive until rank 0 is done
+  if (tid == 0) BST_STAMP(g_k1_trace, 5);
 }
 
 // ---------------------------------------------------------------- launcher
-cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, int64_t row_stride,
-                                int k, int32_t *ids, float *lg, float *q, double *lse, int num_sms,
+cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, int64_t row_stride, int k,
+                                int32_t *ids, float *lg, float *q, double *lse, uint32_t *dev_err, int num_sms,
                                 cudaStream_t stream) {
+  (void)num_sms;
   const int esz = bf16 ? 2 : 4;
-  // CTAs per row: enough clusters to cover the GPU about twice, chunks of at
-  // least 4096 elements, at most 16 CTAs (a non-portable cluster size).
-  int C = 1;
-  while (C < K1_MAXC && static_cast<int64_t>(rows) * C < 2LL * num_sms && V / (2 * C) >= 4096) C <<= 1;
   const int vec = 16 / esz;
+  // CTAs per row: staged chunks of about 48 KB, at most a portable cluster of 8
+  // (very long rows take larger chunks)
+  const int64_t row_bytes = static_cast<int64_t>(V) * esz;
+  int C = static_cast<int>(std::min<int64_t>(K1_MAXC, (row_bytes + K1_CHUNK_BYTES - 1) / K1_CHUNK_BYTES));
+  if (C < 1) C = 1;
   int chunk = (V + C - 1) / C;
   chunk = (chunk + vec - 1) / vec * vec;
-  const bool vec_ok = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((row_stride * esz) % 16 == 0);
+  C = (V + chunk - 1) / chunk;
+  const bool bulk = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((row_stride * esz) % 16 == 0) &&
+                    (row_bytes % 16 == 0) && (static_cast<int64_t>(chunk) * esz <= K1_MAX_SMEM);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, rows, 1);
   cfg.blockDim = dim3(K1_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = bulk ? static_cast<size_t>(chunk) * esz : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -352,25 +352,21 @@ cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+#define BST_K1_ARGS logits, V, row_stride, k, chunk, ids, lg, q, lse, dev_err
   if (bf16) {
-    if (vec_ok)
-      return cudaLaunchKernelEx(&cfg, topk_softmax_kernel<BF16Tag, true>, logits, V, row_stride, k, chunk, ids, lg, q, lse);
-    return cudaLaunchKernelEx(&cfg, topk_softmax_kernel<BF16Tag, false>, logits, V, row_stride, k, chunk, ids, lg, q, lse);
+    if (bulk) return cudaLaunchKernelEx(&cfg, topk_softmax_kernel<BF16Tag, true>, BST_K1_ARGS);
+    return cudaLaunchKernelEx(&cfg, topk_softmax_kernel<BF16Tag, false>, BST_K1_ARGS);
   }
-  if (vec_ok)
-    return cudaLaunchKernelEx(&cfg, topk_softmax_kernel<F32Tag, true>, logits, V, row_stride, k, chunk, ids, lg, q, lse);
-  return cudaLaunchKernelEx(&cfg, topk_softmax_kernel<F32Tag, false>, logits, V, row_stride, k, chunk, ids, lg, q, lse);
+  if (bulk) return cudaLaunchKernelEx(&cfg, topk_softmax_kernel<F32Tag, true>, BST_K1_ARGS);
+  return cudaLaunchKernelEx(&cfg, topk_softmax_kernel<F32Tag, false>, BST_K1_ARGS);
+#undef BST_K1_ARGS
 }
 
 cudaError_t prepare_topk_softmax() {
   cudaError_t e;
-  e = cudaFuncSetAttribute(topk_softmax_kernel<BF16Tag, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  e = cudaFuncSetAttribute(topk_softmax_kernel<BF16Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_MAX_SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(topk_softmax_kernel<BF16Tag, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(topk_softmax_kernel<F32Tag, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(topk_softmax_kernel<F32Tag, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaFuncSetAttribute(topk_softmax_kernel<F32Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_MAX_SMEM);
 }
 
 }  // namespace bst

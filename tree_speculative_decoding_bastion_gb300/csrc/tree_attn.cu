@@ -12,34 +12,48 @@
 // bf16 path (tcgen05): one CTA per (request b, KV head, 128-row M-tile, KV
 // split).  The M rows pack g = Hq/Hkv query heads x tree nodes of one KV head
 // (GQA), so every K/V tile is used by all heads of its group.  Roles:
-//   warp 4      TMA producer: Q once, then K/V tiles (128 keys) into a 2-stage
-//               ring with 128-byte swizzle; paged caches are gathered page by
-//               page through a 4-D tensor map; no multicast.
+//   warp 4      TMA producer: Q once, then K tiles (128 keys, 3-stage ring,
+//               running one tile ahead) and V tiles (2-stage ring), 128-byte
+//               swizzle; paged caches are gathered page by page through a 4-D
+//               tensor map; no multicast.
 //   warp 5      MMA issuer (one thread): S = Q K^T into TMEM (two S buffers),
 //               O += P V with P read from TMEM (P aliases its S buffer).
 //   warps 0-3   softmax: thread r owns TMEM lane r = M-tile row r; it reads S,
 //               applies the context bound or the ancestor bits, keeps the
 //               running max / sum in the log2 domain, writes P (bf16) to TMEM,
-//               rescales O when the max grows, and runs the epilogue.
-// Splits of the context combine in the workspace: the last CTA of a
-// (b, kvh, M-tile) (atomic ticket, no waiting) merges the partial (O, m, l).
+//               and rescales O only when its row max grew by more than 2^8
+//               (the exact result is the same for any running reference max).
+// The KV splits of one (b, kvh, M-tile) form one thread-block cluster: each CTA
+// leaves its partial (O, m, l) in its own shared memory and, after a cluster
+// barrier, every CTA merges a slice of the rows by reading the others' partials
+// over distributed shared memory.  No workspace, no global partials.
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // BASTION_DEVERR_TIMEOUT, drains what it issued and frees its TMEM.
 //
 // f32 path: an exact fp32 flash-decoding kernel, one CTA per (b, node, head).
+#include <cooperative_groups.h>
 #include <math_constants.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "sm100_ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace bst {
 
 constexpr int ATT_THREADS = 192;
-constexpr int ATT_N = 128;            // keys per tile
-constexpr int ATT_M = 128;            // rows per M-tile
-constexpr int ATT_HALF = ATT_N * 128; // bytes of 128 rows x 64 bf16
+constexpr int ATT_N = 128;              // keys per tile
+constexpr int ATT_M = 128;              // rows per M-tile
+constexpr int ATT_HALF = ATT_N * 128;   // bytes of 128 rows x 64 bf16
+constexpr int ATT_KSTAGES = 3;
+constexpr int ATT_VSTAGES = 2;
+constexpr int ATT_MAX_SPLITS = 8;       // a portable cluster
 constexpr uint64_t ATT_WAIT_NS = 200ull * 1000ull * 1000ull;
+constexpr float ATT_RESCALE_LOG2 = 8.f;
 
 struct AttnParams {
   int B, n_max, Hq, Hkv, g, mtiles, splits, tiles_per_split;
@@ -51,23 +65,23 @@ struct AttnParams {
   const unsigned long long *mask;
   const int32_t *block_table;
   uint16_t *out;             // bf16 [B, n_max, Hq, d]
-  float *ws_o;               // [units, splits, 128, d]
-  float2 *ws_ml;             // [units, splits, 128]
-  uint32_t *tickets;         // [units]
   uint32_t *dev_err;
 };
 
 struct AttnBars {
   uint64_t q_full;
-  uint64_t kv_full[2];
-  uint64_t kv_empty[2];
+  uint64_t k_full[ATT_KSTAGES];
+  uint64_t k_empty[ATT_KSTAGES];
+  uint64_t v_full[ATT_VSTAGES];
+  uint64_t v_empty[ATT_VSTAGES];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int last;
+  float part_m[ATT_M];       // this CTA's partial row max (log2 domain)
+  float part_l[ATT_M];       // and row sum, for the cluster merge
 };
 
 template <int D>
@@ -75,10 +89,14 @@ struct AttnLayout {
   static constexpr int NH = D / 64;
   static constexpr int Q_BYTES = NH * ATT_HALF;
   static constexpr int KV_BYTES = NH * ATT_HALF;
-  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   static constexpr int Q_OFF = 0;
-  static constexpr int STAGE_OFF = Q_BYTES;
-  static constexpr int BAR_OFF = STAGE_OFF + 2 * STAGE_BYTES;
+  static constexpr int K_OFF = Q_BYTES;
+  static constexpr int V_OFF = K_OFF + ATT_KSTAGES * KV_BYTES;
+  static constexpr int BAR_OFF = V_OFF + ATT_VSTAGES * KV_BYTES;
+  // the partial O (128 rows x D fp32, stored as [D/4][128] float4) reuses the
+  // K ring once every MMA has finished
+  static constexpr int O_OFF = K_OFF;
+  static_assert(ATT_M * D * 4 <= ATT_KSTAGES * KV_BYTES, "partial O must fit the K ring");
   static constexpr int USED = BAR_OFF + static_cast<int>(sizeof(AttnBars));
   // 1024 bytes of slack for aligning the dynamic shared memory base; at least
   // 120 KB so that a single CTA owns each SM (its TMEM allocation is 512 columns).
@@ -116,6 +134,75 @@ BST_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// 2^x on the special-function unit (the hardware approximation instruction;
+// 2^-inf = 0)
+BST_DEV float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Merge of the S split partials for the rows this CTA owns: rows
+// [split * 128/S, (split + 1) * 128/S), each of the 128 threads one row and D/S
+// columns.  Every remote load is issued before any is used.
+template <int D, int S>
+BST_DEV void merge_splits(const AttnParams &p, cg::cluster_group &cluster, AttnBars *bars, uint8_t *part_o, int b,
+                          int kvh, int mtile, int split, int nb) {
+  constexpr int ROWS = ATT_M / S;
+  constexpr int COLS = D / S;
+  constexpr int C4 = COLS / 4;
+  const int tid = threadIdx.x;
+  if (tid >= 128) return;
+  const int rr = split * ROWS + (tid % ROWS);
+  const int cgp = tid / ROWS;
+  const int prow = mtile * ATT_M + rr;
+  const int nd = prow / p.g;
+  if (nd >= nb) return;
+  float ms[S], ls[S];
+  float4 ov[S][C4];
+#pragma unroll
+  for (int s2 = 0; s2 < S; ++s2) {
+    const AttnBars *ob = cluster.map_shared_rank(bars, s2);
+    ms[s2] = ob->part_m[rr];
+    ls[s2] = ob->part_l[rr];
+    const float4 *src = cluster.map_shared_rank(reinterpret_cast<const float4 *>(part_o), s2);
+#pragma unroll
+    for (int c4 = 0; c4 < C4; ++c4) ov[s2][c4] = src[(cgp * C4 + c4) * ATT_M + rr];
+  }
+  float M = -CUDART_INF_F;
+#pragma unroll
+  for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, ms[s2]);
+  float acc[COLS];
+#pragma unroll
+  for (int e = 0; e < COLS; ++e) acc[e] = 0.f;
+  float lsum = 0.f;
+#pragma unroll
+  for (int s2 = 0; s2 < S; ++s2) {
+    // empty splits carry m = -inf, l = 0 and a zero O
+    const float w = (ms[s2] == -CUDART_INF_F) ? 0.f : ex2(ms[s2] - M);
+    lsum += w * ls[s2];
+#pragma unroll
+    for (int c4 = 0; c4 < C4; ++c4) {
+      acc[4 * c4 + 0] += w * ov[s2][c4].x;
+      acc[4 * c4 + 1] += w * ov[s2][c4].y;
+      acc[4 * c4 + 2] += w * ov[s2][c4].z;
+      acc[4 * c4 + 3] += w * ov[s2][c4].w;
+    }
+  }
+  const float inv = 1.f / lsum;
+  const int hl = prow - nd * p.g;
+  uint16_t *dst = p.out + ((static_cast<int64_t>(b) * p.n_max + nd) * p.Hq + kvh * p.g + hl) * D + cgp * COLS;
+#pragma unroll
+  for (int c = 0; c < COLS; c += 8) {
+    uint4 v;
+    v.x = pack_bf16x2(acc[c + 0] * inv, acc[c + 1] * inv);
+    v.y = pack_bf16x2(acc[c + 2] * inv, acc[c + 3] * inv);
+    v.z = pack_bf16x2(acc[c + 4] * inv, acc[c + 5] * inv);
+    v.w = pack_bf16x2(acc[c + 6] * inv, acc[c + 7] * inv);
+    *reinterpret_cast<uint4 *>(dst + c) = v;
+  }
+}
+
 template <int D, bool kPaged>
 __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -127,18 +214,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   uint8_t *sQ = smem + LY::Q_OFF;
   AttnBars *bars = reinterpret_cast<AttnBars *>(smem + LY::BAR_OFF);
   volatile int *abort = &bars->abort;
+  cg::cluster_group cluster = cg::this_cluster();
 
   const int mtile = blockIdx.x;
-  const int split = blockIdx.y;
+  const int split = blockIdx.y;   // the cluster spans the splits (blockIdx.y)
   const int bh = blockIdx.z;
   const int b = bh / p.Hkv;
   const int kvh = bh - b * p.Hkv;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
-  const int unit = bh * p.mtiles + mtile;
 
   if (tid == 0) BST_TRACE_AT(0);
+  // request-level checks: identical for every CTA of a cluster, so a cluster
+  // leaves together
   const int nb = p.n[b];
   if (nb < 1 || nb > p.n_max) {
     if (tid == 0 && mtile == 0 && split == 0 && kvh == 0) set_err(p.dev_err, BASTION_DEVERR_N);
@@ -161,70 +250,58 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   const int r = tid;   // valid for tid < 128
   const int pidx = mtile * ATT_M + r;
   const int node = pidx / p.g;
-  const int hl = pidx - node * p.g;
   const bool active = (tid < 128) && (node < nb);
 
   float m_run = -CUDART_INF_F;
   float l_run = 0.f;
   bool ok = true;
+  uint32_t tbase = 0;
+
+  if (tid == 0) {
+    mbar_init(&bars->q_full, 1);
+#pragma unroll
+    for (int i = 0; i < ATT_KSTAGES; ++i) mbar_init(&bars->k_full[i], 1), mbar_init(&bars->k_empty[i], 1);
+#pragma unroll
+    for (int i = 0; i < ATT_VSTAGES; ++i) mbar_init(&bars->v_full[i], 1), mbar_init(&bars->v_empty[i], 1);
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->p_full[0], 128);
+    mbar_init(&bars->p_full[1], 128);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (T > 0 && warp == 0) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) BST_TRACE_AT(1);
 
   if (T > 0) {
-    if (tid == 0) {
-      mbar_init(&bars->q_full, 1);
-      mbar_init(&bars->kv_full[0], 1);
-      mbar_init(&bars->kv_full[1], 1);
-      mbar_init(&bars->kv_empty[0], 1);
-      mbar_init(&bars->kv_empty[1], 1);
-      mbar_init(&bars->s_full[0], 1);
-      mbar_init(&bars->s_full[1], 1);
-      mbar_init(&bars->p_full[0], 128);
-      mbar_init(&bars->p_full[1], 128);
-      mbar_init(&bars->o_done, 1);
-      mbar_init(&bars->drain, 1);
-      bars->abort = 0;
-      bars->last = 0;
-      fence_mbar_init();
-    }
-    if (warp == 0) {
-      tmem_alloc(&bars->tmem_base, 512);
-      tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = bars->tmem_base;
+    tbase = bars->tmem_base;
     const uint32_t tO = tbase + 256;
-    if (tid == 0) BST_TRACE_AT(1);
 
     if (warp == 4) {
       // ------------------------------------------------ TMA producer
       if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        tma_prefetch_desc(&tm_kt);
-        tma_prefetch_desc(&tm_vt);
         BST_TRACE_AT(2);
         mbar_expect_tx(&bars->q_full, LY::Q_BYTES);
 #pragma unroll
         for (int h = 0; h < LY::NH; ++h)
           tma_load_3d(sQ + h * ATT_HALF, &tm_q, &bars->q_full, h * 64, kvh * p.g, b * p.n_max + mtile * (ATT_M / p.g));
-        int issued = 0;
-        for (int j = 0; j < T; ++j) {
-          const int st = j & 1;
-          if (j >= 2 && !mbar_wait(&bars->kv_empty[st], ((j >> 1) - 1) & 1, abort, ATT_WAIT_NS)) break;
-          uint8_t *sK = smem + LY::STAGE_OFF + st * LY::STAGE_BYTES;
-          uint8_t *sV = sK + LY::KV_BYTES;
-          uint64_t *fb = &bars->kv_full[st];
-          mbar_expect_tx(fb, LY::STAGE_BYTES);
+        // one K or V tile (context or tree) into `dst`, completing on `fb`
+        auto load_tile = [&](int j, bool is_v, uint8_t *dst, uint64_t *fb) {
+          const CUtensorMap *mc = is_v ? &tm_v : &tm_k;
+          const CUtensorMap *mt = is_v ? &tm_vt : &tm_kt;
           if (j < n_ctx) {
             const int ct = ct0 + j;
             if (!kPaged) {
 #pragma unroll
-              for (int h = 0; h < LY::NH; ++h) {
-                tma_load_3d(sK + h * ATT_HALF, &tm_k, fb, h * 64, ct * ATT_N, b * p.Hkv + kvh);
-                tma_load_3d(sV + h * ATT_HALF, &tm_v, fb, h * 64, ct * ATT_N, b * p.Hkv + kvh);
-              }
+              for (int h = 0; h < LY::NH; ++h) tma_load_3d(dst + h * ATT_HALF, mc, fb, h * 64, ct * ATT_N, b * p.Hkv + kvh);
             } else {
               const int ps = p.page_size;
               for (int pi = 0; pi < ATT_N / ps; ++pi) {
@@ -238,26 +315,46 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
                   }
                 }
 #pragma unroll
-                for (int h = 0; h < LY::NH; ++h) {
-                  tma_load_4d(sK + h * ATT_HALF + pi * ps * 128, &tm_k, fb, h * 64, 0, kvh, page);
-                  tma_load_4d(sV + h * ATT_HALF + pi * ps * 128, &tm_v, fb, h * 64, 0, kvh, page);
-                }
+                for (int h = 0; h < LY::NH; ++h) tma_load_4d(dst + h * ATT_HALF + pi * ps * 128, mc, fb, h * 64, 0, kvh, page);
               }
             }
           } else {
             const int tt = j - n_ctx;
 #pragma unroll
-            for (int h = 0; h < LY::NH; ++h) {
-              tma_load_3d(sK + h * ATT_HALF, &tm_kt, fb, h * 64, kvh, b * p.n_max + tt * ATT_N);
-              tma_load_3d(sV + h * ATT_HALF, &tm_vt, fb, h * 64, kvh, b * p.n_max + tt * ATT_N);
-            }
+            for (int h = 0; h < LY::NH; ++h) tma_load_3d(dst + h * ATT_HALF, mt, fb, h * 64, kvh, b * p.n_max + tt * ATT_N);
           }
-          issued = j + 1;
+        };
+        int k_issued = 0, v_issued = 0;
+        auto issue_k = [&](int j) -> bool {
+          const int st = j % ATT_KSTAGES;
+          if (j >= ATT_KSTAGES && !mbar_wait(&bars->k_empty[st], ((j / ATT_KSTAGES) - 1) & 1, abort, ATT_WAIT_NS))
+            return false;
+          mbar_expect_tx(&bars->k_full[st], LY::KV_BYTES);
+          load_tile(j, false, smem + LY::K_OFF + st * LY::KV_BYTES, &bars->k_full[st]);
+          k_issued = j + 1;
+          return true;
+        };
+        auto issue_v = [&](int j) -> bool {
+          const int st = j % ATT_VSTAGES;
+          if (j >= ATT_VSTAGES && !mbar_wait(&bars->v_empty[st], ((j / ATT_VSTAGES) - 1) & 1, abort, ATT_WAIT_NS))
+            return false;
+          mbar_expect_tx(&bars->v_full[st], LY::KV_BYTES);
+          load_tile(j, true, smem + LY::V_OFF + st * LY::KV_BYTES, &bars->v_full[st]);
+          v_issued = j + 1;
+          return true;
+        };
+        // K runs one tile ahead of V
+        bool run = issue_k(0);
+        for (int j = 0; run && j < T; ++j) {
+          if (j + 1 < T && !issue_k(j + 1)) break;
+          if (!issue_v(j)) break;
         }
         if (*abort) {
           // let the copies already in flight land before the CTA goes away
-          for (int j = max(0, issued - 2); j < issued; ++j)
-            mbar_wait(&bars->kv_full[j & 1], (j >> 1) & 1, abort, ATT_WAIT_NS);
+          for (int j = max(0, k_issued - ATT_KSTAGES); j < k_issued; ++j)
+            mbar_wait(&bars->k_full[j % ATT_KSTAGES], (j / ATT_KSTAGES) & 1, abort, ATT_WAIT_NS);
+          for (int j = max(0, v_issued - ATT_VSTAGES); j < v_issued; ++j)
+            mbar_wait(&bars->v_full[j % ATT_VSTAGES], (j / ATT_VSTAGES) & 1, abort, ATT_WAIT_NS);
           mbar_wait(&bars->q_full, 0, abort, ATT_WAIT_NS);
         }
       }
@@ -270,9 +367,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         bool any = false;
         auto issue_pv = [&](int jj) -> bool {
           const int sb = jj & 1;
+          const int vs = jj % ATT_VSTAGES;
           if (!mbar_wait(&bars->p_full[sb], (jj >> 1) & 1, abort, ATT_WAIT_NS)) return false;
+          if (!mbar_wait(&bars->v_full[vs], (jj / ATT_VSTAGES) & 1, abort, ATT_WAIT_NS)) return false;
           tc_fence_after();
-          const uint32_t v_addr = smem_u32(smem + LY::STAGE_OFF + sb * LY::STAGE_BYTES + LY::KV_BYTES);
+          const uint32_t v_addr = smem_u32(smem + LY::V_OFF + vs * LY::KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < ATT_N / 16; ++kk) {
             // V is the MN-major B operand: 8 keys per 1024-byte swizzle group,
@@ -281,27 +380,30 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
             mma_ts(tO, tbase + sb * 128 + kk * 8, bdesc, IDESC_PV, (jj > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&bars->o_done);
-          mma_commit(&bars->kv_empty[sb]);
+          mma_commit(&bars->v_empty[vs]);
           return true;
         };
         bool run = mbar_wait(&bars->q_full, 0, abort, ATT_WAIT_NS);
         tc_fence_after();
         for (int j = 0; run && j < T; ++j) {
-          const int st = j & 1;
-          if (!mbar_wait(&bars->kv_full[st], (j >> 1) & 1, abort, ATT_WAIT_NS)) { run = false; break; }
+          const int ks = j % ATT_KSTAGES;
+          const int sb = j & 1;
+          if (!mbar_wait(&bars->k_full[ks], (j / ATT_KSTAGES) & 1, abort, ATT_WAIT_NS)) { run = false; break; }
+          // S buffer sb is free once P_{j-2} V_{j-2} (which read P from it) finished
           if (j >= 2 && !mbar_wait(&bars->o_done, (j - 2) & 1, abort, ATT_WAIT_NS)) { run = false; break; }
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + LY::STAGE_OFF + st * LY::STAGE_BYTES);
+          const uint32_t k_addr = smem_u32(smem + LY::K_OFF + ks * LY::KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const int h = kk >> 2;
             const uint32_t off = h * ATT_HALF + (kk & 3) * 32;
             const uint64_t adesc = sdesc_sw128(q_addr + off, 16, 1024);
             const uint64_t bdesc = sdesc_sw128(k_addr + off, 16, 1024);
-            mma_ss(tbase + st * 128, adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
+            mma_ss(tbase + sb * 128, adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
           }
           any = true;
-          mma_commit(&bars->s_full[st]);
+          mma_commit(&bars->s_full[sb]);
+          mma_commit(&bars->k_empty[ks]);
           BST_TRACE_AT(3 + min(j, 7));
           if (j >= 1 && !issue_pv(j - 1)) { run = false; break; }
         }
@@ -321,6 +423,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         const unsigned long long *mrow = p.mask + (static_cast<int64_t>(b) * p.n_max + node) * W;
         for (int w = 0; w < W; ++w) mw[w] = mrow[w];
       }
+      const float cs = p.scale_log2;
       for (int j = 0; j < T; ++j) {
         const int sb = j & 1;
         if (!warp_wait(&bars->s_full[sb], (j >> 1) & 1, abort)) { ok = false; break; }
@@ -335,16 +438,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         tmem_wait_ld32(s + 32);
         tmem_wait_ld32(s + 64);
         tmem_wait_ld32(s + 96);
-        // masking: context tiles bound by L, tree tiles by the ancestor bits;
-        // the scaled, masked scores overwrite s in place
-        float tmax = -CUDART_INF_F;
+        // masking on the raw scores: context tiles are bounded by L, tree
+        // tiles by the ancestor bits (masked scores become -inf)
+        const uint32_t NEG = 0xff800000u;
         if (j < n_ctx) {
           const int nvalid = L - (ct0 + j) * ATT_N;
+          if (nvalid < ATT_N) {
 #pragma unroll
-          for (int c = 0; c < ATT_N; ++c) {
-            const float v = (c < nvalid) ? __uint_as_float(s[c]) * p.scale_log2 : -CUDART_INF_F;
-            s[c] = __float_as_uint(v);
-            tmax = fmaxf(tmax, v);
+            for (int c = 0; c < ATT_N; ++c) s[c] = (c < nvalid) ? s[c] : NEG;
           }
         } else {
           const int tt = j - n_ctx;
@@ -353,28 +454,37 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
 #pragma unroll
           for (int c = 0; c < ATT_N; ++c) {
             const unsigned long long w = (c < 64) ? w0 : w1;
-            const bool vis = ((w >> (c & 63)) & 1ull) != 0ull;
-            const float v = vis ? __uint_as_float(s[c]) * p.scale_log2 : -CUDART_INF_F;
-            s[c] = __float_as_uint(v);
-            tmax = fmaxf(tmax, v);
+            s[c] = ((w >> (c & 63)) & 1ull) ? s[c] : NEG;
           }
         }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
+#pragma unroll
+        for (int c = 8; c < ATT_N; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(s[c]));
+        const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cs;
         const float m_new = fmaxf(m_run, tmax);
-        const float msub = (m_new == -CUDART_INF_F) ? 0.f : m_new;
-        const float alpha = exp2f(m_run - msub);
-        float sum = 0.f;
+        // keep the running reference unless the max grew by more than 2^8
+        const bool jump = m_new > m_run + ATT_RESCALE_LOG2;
+        const float m_use = jump ? m_new : m_run;
+        const float alpha = jump ? ex2(m_run - m_new) : 1.f;
+        const float msub = (m_use == -CUDART_INF_F) ? 0.f : m_use;
+        float sum[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum[i] = 0.f;
         uint32_t pk[ATT_N / 2];
 #pragma unroll
         for (int c = 0; c < ATT_N; c += 2) {
-          const float p0 = exp2f(__uint_as_float(s[c]) - msub);
-          const float p1 = exp2f(__uint_as_float(s[c + 1]) - msub);
-          sum += p0 + p1;
+          const float p0 = ex2(fmaf(__uint_as_float(s[c]), cs, -msub));
+          const float p1 = ex2(fmaf(__uint_as_float(s[c + 1]), cs, -msub));
+          sum[(c >> 1) & 7] += p0 + p1;
           pk[c >> 1] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tbase + lane_off + sb * 128 + 0, pk + 0);
         tmem_st32(tbase + lane_off + sb * 128 + 32, pk + 32);
-        l_run = l_run * alpha + sum;
-        const bool need = (j >= 1) && (alpha != 1.f);
+        l_run = l_run * alpha + (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+        const bool need = (j >= 1) && jump && (m_run > -CUDART_INF_F);
         if (__any_sync(FULL, need)) {
           // O must hold P_{j-1} V_{j-1} before it is rescaled
           if (!warp_wait(&bars->o_done, (j - 1) & 1, abort)) { ok = false; break; }
@@ -393,14 +503,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         tc_fence_before();
         mbar_arrive(&bars->p_full[sb]);
         if (tid == 0) BST_TRACE_AT(19 + min(j, 7));
-        m_run = m_new;
+        m_run = m_use;
       }
-      // ---- epilogue: O after the last P V
-      float o[D];
-      // the drain barrier completes once, after the last P V (and every MMA
-      // before it) has finished
+      // ---- epilogue: O after the last P V (the drain barrier completes once,
+      // after every MMA of this CTA)
       if (ok && !warp_wait(&bars->drain, 0, abort)) ok = false;
       if (tid == 0) BST_TRACE_AT(27);
+      float o[D];
       if (ok) {
         tc_fence_after();
 #pragma unroll
@@ -418,6 +527,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
       if (p.splits == 1) {
         if (ok && active) {
           const float inv = 1.f / l_run;
+          const int hl = pidx - node * p.g;
           uint16_t *dst = p.out + ((static_cast<int64_t>(b) * p.n_max + node) * p.Hq + kvh * p.g + hl) * D;
 #pragma unroll
           for (int c = 0; c < D; c += 8) {
@@ -430,78 +540,45 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
           }
         }
       } else {
-        const int64_t prow = (static_cast<int64_t>(unit) * p.splits + split) * ATT_M + r;
-        float *dst = p.ws_o + prow * D;
+        // partial for the cluster merge: O as [D/4][128 rows] float4 (each
+        // warp writes 512 contiguous bytes per column group), m and l per row
+        float4 *sO = reinterpret_cast<float4 *>(smem + LY::O_OFF);
 #pragma unroll
-        for (int c = 0; c < D; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-        p.ws_ml[prow] = make_float2(ok ? m_run : -CUDART_INF_F, ok ? l_run : 0.f);
-        if (tid == 0) BST_TRACE_AT(28);
+        for (int c = 0; c < D; c += 4) sO[(c >> 2) * ATT_M + r] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        bars->part_m[r] = ok ? m_run : -CUDART_INF_F;
+        bars->part_l[r] = ok ? l_run : 0.f;
       }
+      if (tid == 0) BST_TRACE_AT(28);
     }
-    // all roles done with TMEM
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tbase, 512);
-    if (tid == 0) BST_TRACE_AT(31);
-    if (*abort && tid == 0) set_err(p.dev_err, BASTION_DEVERR_TIMEOUT);
   } else if (p.splits > 1 && tid < 128) {
-    // nothing to attend to in this split: an empty partial
-    const int64_t prow = (static_cast<int64_t>(unit) * p.splits + split) * ATT_M + r;
-    p.ws_ml[prow] = make_float2(-CUDART_INF_F, 0.f);
+    // nothing to attend to in this split: an empty (zero) partial
+    float4 *sO = reinterpret_cast<float4 *>(smem + LY::O_OFF);
+#pragma unroll
+    for (int c = 0; c < D; c += 4) sO[(c >> 2) * ATT_M + r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    bars->part_m[r] = -CUDART_INF_F;
+    bars->part_l[r] = 0.f;
   }
 
-  // ---- split combine: the last CTA of this (b, kvh, M-tile) merges
+  // all roles are done with TMEM
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (T > 0 && warp == 0) tmem_dealloc(tbase, 512);
+  if (T > 0 && *abort && tid == 0) set_err(p.dev_err, BASTION_DEVERR_TIMEOUT);
+
+  // ---- cluster merge of the splits over distributed shared memory
   if (p.splits > 1) {
-    __shared__ int s_last;
-    if (tid < 128) {
-      __threadfence();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (tid == 0) s_last = (atomicAdd(&p.tickets[unit], 1u) == static_cast<uint32_t>(p.splits - 1)) ? 1 : 0;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (s_last) {
-        __threadfence();
-        if (tid == 0) BST_TRACE_AT(29);
-        if (active) {
-          const int64_t base = static_cast<int64_t>(unit) * p.splits * ATT_M + r;
-          float M = -CUDART_INF_F;
-          for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(&p.ws_ml[base + s * ATT_M].x));
-          float acc[D];
-#pragma unroll
-          for (int e = 0; e < D; ++e) acc[e] = 0.f;
-          float lsum = 0.f;
-          for (int s = 0; s < p.splits; ++s) {
-            const float2 ml = __ldcg(&p.ws_ml[base + s * ATT_M]);
-            if (ml.x == -CUDART_INF_F) continue;
-            const float w = exp2f(ml.x - M);
-            lsum += w * ml.y;
-            const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + (base + s * ATT_M) * D);
-#pragma unroll
-            for (int c = 0; c < D / 4; ++c) {
-              const float4 v = __ldcg(src + c);
-              acc[4 * c + 0] += w * v.x;
-              acc[4 * c + 1] += w * v.y;
-              acc[4 * c + 2] += w * v.z;
-              acc[4 * c + 3] += w * v.w;
-            }
-          }
-          const float inv = 1.f / lsum;
-          uint16_t *dst = p.out + ((static_cast<int64_t>(b) * p.n_max + node) * p.Hq + kvh * p.g + hl) * D;
-#pragma unroll
-          for (int c = 0; c < D; c += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(acc[c + 0] * inv, acc[c + 1] * inv);
-            v.y = pack_bf16x2(acc[c + 2] * inv, acc[c + 3] * inv);
-            v.z = pack_bf16x2(acc[c + 4] * inv, acc[c + 5] * inv);
-            v.w = pack_bf16x2(acc[c + 6] * inv, acc[c + 7] * inv);
-            *reinterpret_cast<uint4 *>(dst + c) = v;
-          }
-        }
-        if (tid == 0) p.tickets[unit] = 0u;   // ready for the next call
-        if (tid == 0) BST_TRACE_AT(30);
-      }
+    cluster.sync();
+    if (tid == 0) BST_TRACE_AT(29);
+    switch (p.splits) {
+      case 2: merge_splits<D, 2>(p, cluster, bars, smem + LY::O_OFF, b, kvh, mtile, split, nb); break;
+      case 4: merge_splits<D, 4>(p, cluster, bars, smem + LY::O_OFF, b, kvh, mtile, split, nb); break;
+      default: merge_splits<D, 8>(p, cluster, bars, smem + LY::O_OFF, b, kvh, mtile, split, nb); break;
     }
+    if (tid == 0) BST_TRACE_AT(30);
+    cluster.sync();   // the partials stay readable until every CTA has merged
   }
+  if (tid == 0) BST_TRACE_AT(31);
 }
 
 // ------------------------------------------------------------------ fp32 path
@@ -623,28 +700,70 @@ struct AttnPlan {
   size_t ws_bytes, off_o, off_ml;
 };
 
-AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, int num_sms) {
+// Clusters of `splits` CTAs of the bf16 kernel that the current device keeps
+// resident at once (cached per device, head_dim, layout and cluster size).
+static int max_active_clusters(int d, bool paged, int splits) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, d, paged ? 1 : 0, splits);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, splits, 1);
+  cfg.blockDim = dim3(ATT_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = d == 128 ? AttnLayout<128>::SMEM : AttnLayout<64>::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = splits;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const void *fn = d == 128 ? (paged ? reinterpret_cast<const void *>(tree_attn_tc_kernel<128, true>)
+                                     : reinterpret_cast<const void *>(tree_attn_tc_kernel<128, false>))
+                            : (paged ? reinterpret_cast<const void *>(tree_attn_tc_kernel<64, true>)
+                                     : reinterpret_cast<const void *>(tree_attn_tc_kernel<64, false>));
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
+
+AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, int num_sms, bool paged) {
   AttnPlan pl{};
   const int g = Hq / Hkv;
   pl.mtiles = (n_max * g + ATT_M - 1) / ATT_M;
   pl.cap = cap;
   const int64_t ctx_tiles = (cap + ATT_N - 1) / ATT_N;
+  const int64_t tree_tiles = (n_max + ATT_N - 1) / ATT_N;
   const int64_t units = static_cast<int64_t>(B) * Hkv * pl.mtiles;
-  // enough CTAs to fill the GPU about twice, at least 4 tiles per split
-  int64_t splits = (2LL * num_sms + units - 1) / units;
-  splits = std::min<int64_t>(splits, std::max<int64_t>(1, ctx_tiles / 4));
-  splits = std::max<int64_t>(1, std::min<int64_t>(splits, 64));
-  pl.splits = static_cast<int>(splits);
-  pl.tiles_per_split = static_cast<int>((ctx_tiles + splits - 1) / splits);
-  if (pl.tiles_per_split == 0) pl.tiles_per_split = 1;
-  if (pl.splits == 1) {
-    pl.ws_bytes = 0;
-  } else {
-    const size_t t = (static_cast<size_t>(units) * 4 + 255) / 256 * 256;
-    pl.off_o = t;
-    pl.off_ml = t + static_cast<size_t>(units) * pl.splits * ATT_M * d * 4;
-    pl.ws_bytes = pl.off_ml + static_cast<size_t>(units) * pl.splits * ATT_M * 8;
+  // KV splits per (b, kvh, M-tile): the power of two up to a portable cluster
+  // of 8 that minimises (waves of resident clusters) x (tiles per CTA + a
+  // fixed cost of about four tiles for set-up, first loads and the merge)
+  int best = 1;
+  double best_cost = 1e30;
+  for (int s = 1; s <= ATT_MAX_SPLITS; s <<= 1) {
+    if (s > 1 && ctx_tiles < 2LL * s) break;
+    int per_wave = (s == 1) ? num_sms : max_active_clusters(d, paged, s);
+    if (per_wave < 1) continue;
+    const int64_t waves = (units + per_wave - 1) / per_wave;
+    const double cost = static_cast<double>(waves) * (4.0 + (ctx_tiles + s - 1) / s + tree_tiles);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
   }
+  pl.splits = best;
+  pl.tiles_per_split = static_cast<int>((ctx_tiles + best - 1) / best);
+  if (pl.tiles_per_split == 0) pl.tiles_per_split = 1;
+  pl.ws_bytes = 0;   // the splits merge inside their cluster
+  pl.off_o = pl.off_ml = 0;
   return pl;
 }
 
@@ -664,6 +783,7 @@ cudaError_t launch_tree_attn_tc(const CUtensorMap *maps, const AttnPlan &pl, int
                                 const int32_t *ctx_len, const int32_t *n, const uint64_t *mask,
                                 const int32_t *block_table, void *out, void *ws, uint32_t *dev_err,
                                 cudaStream_t stream) {
+  (void)ws;
   AttnParams p{};
   p.B = B;
   p.n_max = n_max;
@@ -683,25 +803,25 @@ cudaError_t launch_tree_attn_tc(const CUtensorMap *maps, const AttnPlan &pl, int
   p.mask = reinterpret_cast<const unsigned long long *>(mask);
   p.block_table = block_table;
   p.out = reinterpret_cast<uint16_t *>(out);
-  if (pl.splits > 1) {
-    p.tickets = reinterpret_cast<uint32_t *>(ws);
-    p.ws_o = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + pl.off_o);
-    p.ws_ml = reinterpret_cast<float2 *>(reinterpret_cast<char *>(ws) + pl.off_ml);
-  }
   p.dev_err = dev_err;
-  dim3 grid(pl.mtiles, pl.splits, B * Hkv);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.mtiles, pl.splits, B * Hkv);
+  cfg.blockDim = dim3(ATT_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = d == 128 ? AttnLayout<128>::SMEM : AttnLayout<64>::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = pl.splits;   // the splits of one (b, kvh, M-tile) form a cluster
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (d == 128) {
-    if (paged)
-      tree_attn_tc_kernel<128, true><<<grid, ATT_THREADS, AttnLayout<128>::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
-    else
-      tree_attn_tc_kernel<128, false><<<grid, ATT_THREADS, AttnLayout<128>::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
-  } else {
-    if (paged)
-      tree_attn_tc_kernel<64, true><<<grid, ATT_THREADS, AttnLayout<64>::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
-    else
-      tree_attn_tc_kernel<64, false><<<grid, ATT_THREADS, AttnLayout<64>::SMEM, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    if (paged) return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128, true>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128, false>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
   }
-  return cudaGetLastError();
+  if (paged) return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<64, true>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<64, false>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
 }
 
 cudaError_t launch_tree_attn_f32(const float *q, const float *kt, const float *vt, const float *kc, const float *vc,

@@ -160,20 +160,25 @@ def _drafter_row(wl: Workload, rng: np.random.Generator) -> np.ndarray:
         x[t] += np.float32(np.log(9.0) + np.log(V) + 0.5)
         return x
     if wl.logits == "flat":
-        # Temperature T chosen by bisection so that the largest share
-        # e^{z_max/T} / sum_u e^{z_u/T} is 0.30; this calibrates the input only.
-        zd = z.astype(np.float64)
-        zmax = zd.max()
-        lo, hi = 1e-3, 10.0
-        for _ in range(40):
-            T = 0.5 * (lo + hi)
-            share = 1.0 / np.sum(np.exp((zd - zmax) / T))
-            if share > 0.30:
-                lo = T      # too peaked: raise the temperature
-            else:
-                hi = T
-        return (zd / (0.5 * (lo + hi))).astype(np.float32)
+        return z   # scaled by a per-row temperature in flat_rows()
     raise ValueError(f"unknown logit regime {wl.logits!r}")
+
+
+def flat_rows(z: np.ndarray) -> np.ndarray:
+    """Per-row temperature T (bisection on log T, all rows at once) so that the
+    largest share e^{z_max/T} / sum_u e^{z_u/T} is 0.30; returns z / T.  This
+    calibrates the input only."""
+    z = np.asarray(z, dtype=np.float32)
+    d = z - z.max(axis=1, keepdims=True)
+    lo = np.full((z.shape[0], 1), np.log(1e-3), dtype=np.float32)
+    hi = np.full((z.shape[0], 1), np.log(10.0), dtype=np.float32)
+    for _ in range(26):
+        mid = 0.5 * (lo + hi)
+        share = 1.0 / np.exp(d / np.exp(mid)).sum(axis=1, keepdims=True)
+        too_peaked = share > 0.30
+        lo = np.where(too_peaked, mid, lo)
+        hi = np.where(too_peaked, hi, mid)
+    return (z / np.exp(0.5 * (lo + hi))).astype(np.float32)
 
 
 @dataclass
@@ -233,6 +238,8 @@ def make_step_inputs(wl: Workload, seed: int, *, with_attention: bool = True,
         sb = seed if req_seeds is None else int(req_seeds[b])
         for k in range(K):
             logits32[b, k] = _drafter_row(wl, _rng(sb, 1, b, k))
+    if wl.logits == "flat":
+        logits32 = flat_rows(logits32.reshape(B * K, V)).reshape(B, K, V)
     r = _rng(seed, 2)
     root_tok = r.integers(0, V, size=B).astype(np.int32)
     if wl.L_min > 0:
