@@ -114,7 +114,8 @@ def attention_rows(inp, tree, count, seed=0, groups=4):
         for i in {0, nb - 1, nb // 2}:
             for h in heads:
                 rows.add((b, i, h))
-    while len(rows) < count:
+    available = sum(int(tree["n"][b]) * wl.g for (b, _) in pick)
+    while len(rows) < min(count, available):
         b, kvh = pick[int(rng.integers(len(pick)))]
         rows.add((b, int(rng.integers(int(tree["n"][b]))), kvh * wl.g + int(rng.integers(wl.g))))
     return sorted(rows)

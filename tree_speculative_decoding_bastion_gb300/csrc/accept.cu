@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
   __shared__ uint64_t s_bar;
   __shared__ unsigned long long s_red[K4_WARPS];
   __shared__ int s_last;
+  __shared__ int32_t s_am[BASTION_MAX_NODES], s_par[BASTION_MAX_NODES], s_tok[BASTION_MAX_NODES];
 
   const int crank = blockIdx.x;
   const int row = blockIdx.y;
@@ -58,6 +59,13 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   if (tid == 0) BST_STAMP(g_k4_trace, 0);
+  if (kBulk && tid == 0) {
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 0) BST_STAMP(g_k4_trace, 5);
   const int nb = n_g[b];
 
   if (nb < 1 || nb > n_max) {   // the whole request is invalid
@@ -85,11 +93,7 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
   if (kBulk) {
     // ---- stage the chunk into shared memory with bulk copies
     const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
-    if (tid == 0) {
-      mbar_init(&s_bar, 1);
-      fence_mbar_init();
-    }
-    __syncthreads();
+    __syncthreads();   // the barrier was initialised before the dependency wait
     if (tid == 0 && bytes > 0) {
       mbar_expect_tx(&s_bar, bytes);
       for (uint32_t off = 0; off < bytes; off += 16384u) {
@@ -144,22 +148,29 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
   if (!s_last) return;
 
   // ---- this CTA completed the request: argmax per node, then walk the tree
+  // (the request's argmax, parent and token rows are staged in shared memory
+  // first, so the walk itself touches no global memory)
   __threadfence();
   unsigned long long *rk = rowkey + static_cast<int64_t>(b) * n_max;
-  if (argmax_out)
-    for (int j = tid; j < nb; j += K4_THREADS) argmax_out[static_cast<int64_t>(b) * n_max + j] = packed_i(__ldcg(rk + j));
+  for (int j = tid; j < nb; j += K4_THREADS) {
+    const int32_t am = packed_i(__ldcg(rk + j));
+    s_am[j] = am;
+    s_par[j] = parent[static_cast<int64_t>(b) * n_max + j];
+    s_tok[j] = token[static_cast<int64_t>(b) * n_max + j];
+    if (argmax_out) argmax_out[static_cast<int64_t>(b) * n_max + j] = am;
+  }
+  __syncthreads();
   if (tid < 32) {
-    const int32_t *par = parent + static_cast<int64_t>(b) * n_max;
-    const int32_t *tk = token + static_cast<int64_t>(b) * n_max;
     int u = 0;
     int len2 = 0;
-    int32_t a = packed_i(__ldcg(rk));
+    int32_t a = s_am[0];
     if (lane == 0) acc_nodes[b * (K + 1)] = 0;
     while (len2 < K) {
+      // children come after their parent in the best-first order
       int found = -1;
-      for (int v0 = 1; v0 < nb; v0 += 32) {
+      for (int v0 = u + 1; v0 < nb; v0 += 32) {
         const int v = v0 + lane;
-        const bool hit = (v < nb) && (par[v] == u) && (tk[v] == a);
+        const bool hit = (v < nb) && (s_par[v] == u) && (s_tok[v] == a);
         const unsigned m = __ballot_sync(FULL, hit);
         if (m) {
           found = v0 + __ffs(m) - 1;
@@ -173,7 +184,7 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
         acc_tok[b * (K + 1) + len2 - 1] = a;
       }
       u = found;
-      a = packed_i(__ldcg(rk + u));
+      a = s_am[u];
     }
     if (lane == 0) {
       acc_len[b] = len2;
@@ -212,26 +223,35 @@ cudaError_t launch_accept(const void *target, bool bf16, int B, int n_max, int V
                     ((static_cast<int64_t>(V) * esz) % 16 == 0);
   uint32_t *tickets = reinterpret_cast<uint32_t *>(ws);
   auto *rowkey = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(ws) + accept_ticket_bytes(B));
-  const dim3 grid(C, rows, 1);
-  const size_t smem = bulk ? static_cast<size_t>(chunk) * esz : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, rows, 1);
+  cfg.blockDim = dim3(K4_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = bulk ? static_cast<size_t>(chunk) * esz : 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  cfg.attrs = attr;
+  cfg.numAttrs = fill_launch_attrs(attr);
 #define BST_ACCEPT_ARGS target, n_max, V, row_stride, K, chunk, C, n, parent, token, acc_len, acc_nodes, acc_tok, \
                         bonus, argmax_out, tickets, rowkey, dev_err
   if (bf16) {
-    if (bulk) accept_kernel<BF16Tag, true><<<grid, K4_THREADS, smem, stream>>>(BST_ACCEPT_ARGS);
-    else accept_kernel<BF16Tag, false><<<grid, K4_THREADS, 0, stream>>>(BST_ACCEPT_ARGS);
-  } else {
-    if (bulk) accept_kernel<F32Tag, true><<<grid, K4_THREADS, smem, stream>>>(BST_ACCEPT_ARGS);
-    else accept_kernel<F32Tag, false><<<grid, K4_THREADS, 0, stream>>>(BST_ACCEPT_ARGS);
+    if (bulk) return cudaLaunchKernelEx(&cfg, accept_kernel<BF16Tag, true>, BST_ACCEPT_ARGS);
+    return cudaLaunchKernelEx(&cfg, accept_kernel<BF16Tag, false>, BST_ACCEPT_ARGS);
   }
+  if (bulk) return cudaLaunchKernelEx(&cfg, accept_kernel<F32Tag, true>, BST_ACCEPT_ARGS);
+  return cudaLaunchKernelEx(&cfg, accept_kernel<F32Tag, false>, BST_ACCEPT_ARGS);
 #undef BST_ACCEPT_ARGS
-  return cudaGetLastError();
 }
 
 cudaError_t prepare_accept() {
   cudaError_t e;
   e = cudaFuncSetAttribute(accept_kernel<BF16Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K4_MAX_CHUNK_BYTES);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(accept_kernel<F32Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K4_MAX_CHUNK_BYTES);
+  e = cudaFuncSetAttribute(accept_kernel<F32Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K4_MAX_CHUNK_BYTES);
+  if (e != cudaSuccess) return e;
+  if ((e = prefer_max_shared(accept_kernel<BF16Tag, true>)) != cudaSuccess) return e;
+  if ((e = prefer_max_shared(accept_kernel<BF16Tag, false>)) != cudaSuccess) return e;
+  if ((e = prefer_max_shared(accept_kernel<F32Tag, true>)) != cudaSuccess) return e;
+  return prefer_max_shared(accept_kernel<F32Tag, false>);
 }
 
 }  // namespace bst

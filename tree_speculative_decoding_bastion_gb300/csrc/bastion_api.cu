@@ -17,6 +17,7 @@ namespace bst {
 cudaError_t prepare_topk_softmax();
 cudaError_t prepare_accept();
 cudaError_t prepare_tree_attn();
+cudaError_t prepare_tree_build();
 cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, int64_t row_stride, int k,
                                 int32_t *ids, float *lg, float *q, double *lse, uint32_t *dev_err, int num_sms,
                                 cudaStream_t stream);
@@ -93,11 +94,12 @@ void init_device(int device, DeviceState &st) {
   cudaError_t e1 = bst::prepare_topk_softmax();
   cudaError_t e2 = bst::prepare_accept();
   cudaError_t e3 = bst::prepare_tree_attn();
+  cudaError_t e4 = bst::prepare_tree_build();
   if (prev >= 0) cudaSetDevice(prev);
-  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+  const cudaError_t ea = e1 != cudaSuccess ? e1 : e2 != cudaSuccess ? e2 : e3 != cudaSuccess ? e3 : e4;
+  if (ea != cudaSuccess) {
     st.status = BASTION_ERR_CUDA;
-    st.why = std::string("setting kernel attributes failed: ") +
-             cudaGetErrorString(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
+    st.why = std::string("setting kernel attributes failed: ") + cudaGetErrorString(ea);
     return;
   }
   std::call_once(g_encode_once, [] {

@@ -170,6 +170,44 @@ BST_DEV void set_err(uint32_t *err, uint32_t bit) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Programmatic dependent launch.  The four stages run back to back on one
+// stream and each is launched with programmatic stream serialization, so the
+// next grid may be scheduled while this one still runs.  pdl_wait() blocks
+// until every grid this one depends on has completed and its writes are
+// visible: a kernel calls it before its first global read or write of data a
+// predecessor may touch, and does only private set-up (shared memory,
+// barriers, descriptor prefetch) before it.  pdl_trigger() lets the next grid
+// start launching; it does not publish anything, so it may come early.
+// Without the launch attribute both are no-ops.
+BST_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+BST_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Host side: the launch attributes every stage uses (programmatic
+// serialization, plus a cluster shape when cluster_x > 0).  `attrs` must have
+// room for two entries; returns how many were filled.
+inline unsigned fill_launch_attrs(cudaLaunchAttribute *attrs, int cluster_x = 0, int cluster_y = 1) {
+  unsigned n = 0;
+  attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 0) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = cluster_x;
+    attrs[n].val.clusterDim.y = cluster_y;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  return n;
+}
+
+// Host side: every kernel prefers the largest shared-memory carveout, so
+// consecutive stages never need the SM's L1/shared split to be reconfigured.
+template <class F>
+inline cudaError_t prefer_max_shared(F *fn) {
+  return cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
+}
+
 BST_DEV uint64_t now_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

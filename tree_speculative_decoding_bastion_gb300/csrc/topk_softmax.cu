@@ -38,7 +38,7 @@ extern "C" cudaError_t bastion_trace_read_topk(void *dst, size_t bytes) {
 }
 #endif
 
-constexpr int K1_THREADS = 256;
+constexpr int K1_THREADS = 512;   // 4 warps per scheduler hide the MUFU / shared-memory latency
 constexpr int K1_WARPS = K1_THREADS / 32;
 constexpr int K1_CAP = 1024;                      // candidate buffer
 constexpr int K1_MAXC = 8;                        // CTAs per cluster (row), portable
@@ -49,7 +49,7 @@ constexpr uint64_t K1_WAIT_NS = 200ull * 1000ull * 1000ull;
 struct K1Smem {
   uint64_t bar;
   float wmax[K1_WARPS];
-  float wa[K1_WARPS];          // per warp: ceil(k/8)-th largest lane maximum
+  float wa[K1_WARPS];          // per warp: ceil(k/K1_WARPS)-th largest lane maximum
   float wb[K1_WARPS];          // per warp: k-th largest lane maximum
   float wsum[K1_WARPS];
   int cnt;
@@ -166,6 +166,9 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
     }
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 0) BST_STAMP(g_k1_trace, 6);
   bool staged = true;
   if (kBulk) {
     const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
@@ -345,13 +348,9 @@ cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, 
   cfg.blockDim = dim3(K1_THREADS, 1, 1);
   cfg.dynamicSmemBytes = bulk ? static_cast<size_t>(chunk) * esz : 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = fill_launch_attrs(attr, C, 1);
 #define BST_K1_ARGS logits, V, row_stride, k, chunk, ids, lg, q, lse, dev_err
   if (bf16) {
     if (bulk) return cudaLaunchKernelEx(&cfg, topk_softmax_kernel<BF16Tag, true>, BST_K1_ARGS);
@@ -366,7 +365,12 @@ cudaError_t prepare_topk_softmax() {
   cudaError_t e;
   e = cudaFuncSetAttribute(topk_softmax_kernel<BF16Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_MAX_SMEM);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(topk_softmax_kernel<F32Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_MAX_SMEM);
+  e = cudaFuncSetAttribute(topk_softmax_kernel<F32Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_MAX_SMEM);
+  if (e != cudaSuccess) return e;
+  if ((e = prefer_max_shared(topk_softmax_kernel<BF16Tag, true>)) != cudaSuccess) return e;
+  if ((e = prefer_max_shared(topk_softmax_kernel<BF16Tag, false>)) != cudaSuccess) return e;
+  if ((e = prefer_max_shared(topk_softmax_kernel<F32Tag, true>)) != cudaSuccess) return e;
+  return prefer_max_shared(topk_softmax_kernel<F32Tag, false>);
 }
 
 }  // namespace bst

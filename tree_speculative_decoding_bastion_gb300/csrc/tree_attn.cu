@@ -50,7 +50,8 @@ constexpr int ATT_N = 128;              // keys per tile
 constexpr int ATT_M = 128;              // rows per M-tile
 constexpr int ATT_HALF = ATT_N * 128;   // bytes of 128 rows x 64 bf16
 constexpr int ATT_KSTAGES = 3;
-constexpr int ATT_VSTAGES = 2;
+constexpr int ATT_VSTAGES = 3;
+constexpr int ATT_SBUF = 3;             // S / P buffers in TMEM (128 columns each; O follows)
 constexpr int ATT_MAX_SPLITS = 8;       // a portable cluster
 constexpr uint64_t ATT_WAIT_NS = 200ull * 1000ull * 1000ull;
 constexpr float ATT_RESCALE_LOG2 = 8.f;
@@ -74,8 +75,9 @@ struct AttnBars {
   uint64_t k_empty[ATT_KSTAGES];
   uint64_t v_full[ATT_VSTAGES];
   uint64_t v_empty[ATT_VSTAGES];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t s_full[ATT_SBUF];
+  uint64_t p_full[ATT_SBUF];
+  uint64_t s_free[ATT_SBUF];   // the P V that read buffer b finished
   uint64_t o_done;
   uint64_t drain;
   uint32_t tmem_base;
@@ -101,17 +103,19 @@ struct AttnLayout {
   // 1024 bytes of slack for aligning the dynamic shared memory base; at least
   // 120 KB so that a single CTA owns each SM (its TMEM allocation is 512 columns).
   static constexpr int SMEM = (USED + 1024) > 120 * 1024 ? (USED + 1024) : 120 * 1024;
+  static_assert(SMEM <= 227 * 1024, "exceeds the shared memory of one CTA");
+  static_assert(ATT_SBUF * 128 + D <= 512, "S buffers and O must fit the 512 TMEM columns");
 };
 
 // Optional phase trace (compiled in with -DBST_TRACE only): %globaltimer
-// stamps at the pipeline's phase boundaries, 32 per CTA, read back with
+// stamps at the pipeline's phase boundaries, 64 per CTA, read back with
 // bastion_trace_read().  Normal builds contain none of it.
 #ifdef BST_TRACE
-__device__ unsigned long long g_attn_trace[4096 * 32];
+__device__ unsigned long long g_attn_trace[4096 * 64];
 #define BST_TRACE_AT(ev)                                                                                  \
   do {                                                                                                  \
     const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);               \
-    if (cta_ < 4096u && (ev) < 32) g_attn_trace[cta_ * 32u + (ev)] = globaltimer_ns();                 \
+    if (cta_ < 4096u && (ev) < 64) g_attn_trace[cta_ * 64u + (ev)] = globaltimer_ns();                 \
   } while (0)
 extern "C" cudaError_t bastion_trace_read(void *dst, size_t bytes) {
   return cudaMemcpyFromSymbol(dst, g_attn_trace, bytes);
@@ -148,18 +152,25 @@ BST_DEV float ex2(float x) {
 template <int D, int S>
 BST_DEV void merge_splits(const AttnParams &p, cg::cluster_group &cluster, AttnBars *bars, uint8_t *part_o, int b,
                           int kvh, int mtile, int split, int nb) {
-  constexpr int ROWS = ATT_M / S;
-  constexpr int COLS = D / S;
-  constexpr int C4 = COLS / 4;
+  // this CTA merges R rows with all of its threads: G threads share a row,
+  // each taking CPG of the row's D/4 float4 columns (consecutive threads take
+  // consecutive rows, so the partials are read without bank conflicts).  All
+  // remote loads are issued before any of them is used: one round trip.
+  constexpr int R = (ATT_M + S - 1) / S;
+  constexpr int G = ATT_THREADS / R;
+  constexpr int NC4 = D / 4;
+  constexpr int CPG = (NC4 + G - 1) / G;
   const int tid = threadIdx.x;
-  if (tid >= 128) return;
-  const int rr = split * ROWS + (tid % ROWS);
-  const int cgp = tid / ROWS;
+  if (tid >= R * G) return;
+  const int rr = split * R + (tid % R);
+  if (rr >= ATT_M) return;
+  const int g = tid / R;
+  const int c40 = g * CPG;
   const int prow = mtile * ATT_M + rr;
   const int nd = prow / p.g;
   if (nd >= nb) return;
   float ms[S], ls[S];
-  float4 ov[S][C4];
+  float4 ov[S][CPG];
 #pragma unroll
   for (int s2 = 0; s2 < S; ++s2) {
     const AttnBars *ob = cluster.map_shared_rank(bars, s2);
@@ -167,14 +178,15 @@ BST_DEV void merge_splits(const AttnParams &p, cg::cluster_group &cluster, AttnB
     ls[s2] = ob->part_l[rr];
     const float4 *src = cluster.map_shared_rank(reinterpret_cast<const float4 *>(part_o), s2);
 #pragma unroll
-    for (int c4 = 0; c4 < C4; ++c4) ov[s2][c4] = src[(cgp * C4 + c4) * ATT_M + rr];
+    for (int c = 0; c < CPG; ++c)
+      ov[s2][c] = (c40 + c < NC4) ? src[(c40 + c) * ATT_M + rr] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float M = -CUDART_INF_F;
 #pragma unroll
   for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, ms[s2]);
-  float acc[COLS];
+  float4 acc[CPG];
 #pragma unroll
-  for (int e = 0; e < COLS; ++e) acc[e] = 0.f;
+  for (int c = 0; c < CPG; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float lsum = 0.f;
 #pragma unroll
   for (int s2 = 0; s2 < S; ++s2) {
@@ -182,24 +194,24 @@ BST_DEV void merge_splits(const AttnParams &p, cg::cluster_group &cluster, AttnB
     const float w = (ms[s2] == -CUDART_INF_F) ? 0.f : ex2(ms[s2] - M);
     lsum += w * ls[s2];
 #pragma unroll
-    for (int c4 = 0; c4 < C4; ++c4) {
-      acc[4 * c4 + 0] += w * ov[s2][c4].x;
-      acc[4 * c4 + 1] += w * ov[s2][c4].y;
-      acc[4 * c4 + 2] += w * ov[s2][c4].z;
-      acc[4 * c4 + 3] += w * ov[s2][c4].w;
+    for (int c = 0; c < CPG; ++c) {
+      acc[c].x += w * ov[s2][c].x;
+      acc[c].y += w * ov[s2][c].y;
+      acc[c].z += w * ov[s2][c].z;
+      acc[c].w += w * ov[s2][c].w;
     }
   }
   const float inv = 1.f / lsum;
   const int hl = prow - nd * p.g;
-  uint16_t *dst = p.out + ((static_cast<int64_t>(b) * p.n_max + nd) * p.Hq + kvh * p.g + hl) * D + cgp * COLS;
+  uint16_t *dst = p.out + ((static_cast<int64_t>(b) * p.n_max + nd) * p.Hq + kvh * p.g + hl) * D;
 #pragma unroll
-  for (int c = 0; c < COLS; c += 8) {
-    uint4 v;
-    v.x = pack_bf16x2(acc[c + 0] * inv, acc[c + 1] * inv);
-    v.y = pack_bf16x2(acc[c + 2] * inv, acc[c + 3] * inv);
-    v.z = pack_bf16x2(acc[c + 4] * inv, acc[c + 5] * inv);
-    v.w = pack_bf16x2(acc[c + 6] * inv, acc[c + 7] * inv);
-    *reinterpret_cast<uint4 *>(dst + c) = v;
+  for (int c = 0; c < CPG; ++c) {
+    if (c40 + c < NC4) {
+      uint2 v;
+      v.x = pack_bf16x2(acc[c].x * inv, acc[c].y * inv);
+      v.y = pack_bf16x2(acc[c].z * inv, acc[c].w * inv);
+      *reinterpret_cast<uint2 *>(dst + (c40 + c) * 4) = v;
+    }
   }
 }
 
@@ -226,6 +238,31 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   const int tid = threadIdx.x;
 
   if (tid == 0) BST_TRACE_AT(0);
+  // private set-up first (barriers, descriptor prefetch), then the wait for
+  // the grid that produced the tree
+  if (tid == 0) {
+    mbar_init(&bars->q_full, 1);
+#pragma unroll
+    for (int i = 0; i < ATT_KSTAGES; ++i) mbar_init(&bars->k_full[i], 1), mbar_init(&bars->k_empty[i], 1);
+#pragma unroll
+    for (int i = 0; i < ATT_VSTAGES; ++i) mbar_init(&bars->v_full[i], 1), mbar_init(&bars->v_empty[i], 1);
+#pragma unroll
+    for (int i = 0; i < ATT_SBUF; ++i)
+      mbar_init(&bars->s_full[i], 1), mbar_init(&bars->p_full[i], 128), mbar_init(&bars->s_free[i], 1);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_kt);
+    tma_prefetch_desc(&tm_vt);
+  }
+  pdl_wait();
+  pdl_trigger();
   // request-level checks: identical for every CTA of a cluster, so a cluster
   // leaves together
   const int nb = p.n[b];
@@ -240,10 +277,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   }
   if (mtile * ATT_M >= nb * p.g) return;   // no active row in this M-tile
 
+  // the request's context tiles followed by its tree tiles, spread evenly
+  // over the splits: this split takes tiles [g0, g1)
   const int ctx_tiles = (L + ATT_N - 1) / ATT_N;
-  const int ct0 = split * p.tiles_per_split;
-  const int n_ctx = max(0, min(ctx_tiles, ct0 + p.tiles_per_split) - ct0);
-  const int n_tree = (split == 0) ? (nb + ATT_N - 1) / ATT_N : 0;
+  const int tot_tiles = ctx_tiles + (nb + ATT_N - 1) / ATT_N;
+  const int g0 = (split * tot_tiles) / p.splits;
+  const int g1 = ((split + 1) * tot_tiles) / p.splits;
+  const int ct0 = g0;                                     // first context tile
+  const int n_ctx = max(0, min(g1, ctx_tiles) - g0);
+  const int tr0 = max(g0, ctx_tiles) - ctx_tiles;         // first tree tile
+  const int n_tree = max(0, g1 - max(g0, ctx_tiles));
   const int T = n_ctx + n_tree;
 
   // row owned by a softmax thread
@@ -257,21 +300,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   bool ok = true;
   uint32_t tbase = 0;
 
-  if (tid == 0) {
-    mbar_init(&bars->q_full, 1);
-#pragma unroll
-    for (int i = 0; i < ATT_KSTAGES; ++i) mbar_init(&bars->k_full[i], 1), mbar_init(&bars->k_empty[i], 1);
-#pragma unroll
-    for (int i = 0; i < ATT_VSTAGES; ++i) mbar_init(&bars->v_full[i], 1), mbar_init(&bars->v_empty[i], 1);
-    mbar_init(&bars->s_full[0], 1);
-    mbar_init(&bars->s_full[1], 1);
-    mbar_init(&bars->p_full[0], 128);
-    mbar_init(&bars->p_full[1], 128);
-    mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->drain, 1);
-    bars->abort = 0;
-    fence_mbar_init();
-  }
   if (T > 0 && warp == 0) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
@@ -283,7 +311,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
 
   if (T > 0) {
     tbase = bars->tmem_base;
-    const uint32_t tO = tbase + 256;
+    const uint32_t tO = tbase + ATT_SBUF * 128;
 
     if (warp == 4) {
       // ------------------------------------------------ TMA producer
@@ -319,7 +347,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
               }
             }
           } else {
-            const int tt = j - n_ctx;
+            const int tt = tr0 + j - n_ctx;
 #pragma unroll
             for (int h = 0; h < LY::NH; ++h) tma_load_3d(dst + h * ATT_HALF, mt, fb, h * 64, kvh, b * p.n_max + tt * ATT_N);
           }
@@ -331,6 +359,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
             return false;
           mbar_expect_tx(&bars->k_full[st], LY::KV_BYTES);
           load_tile(j, false, smem + LY::K_OFF + st * LY::KV_BYTES, &bars->k_full[st]);
+          if (j < 8) BST_TRACE_AT(32 + j);
           k_issued = j + 1;
           return true;
         };
@@ -340,6 +369,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
             return false;
           mbar_expect_tx(&bars->v_full[st], LY::KV_BYTES);
           load_tile(j, true, smem + LY::V_OFF + st * LY::KV_BYTES, &bars->v_full[st]);
+          if (j < 8) BST_TRACE_AT(48 + j);
           v_issued = j + 1;
           return true;
         };
@@ -366,10 +396,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         const uint32_t q_addr = smem_u32(sQ);
         bool any = false;
         auto issue_pv = [&](int jj) -> bool {
-          const int sb = jj & 1;
+          const int sb = jj % ATT_SBUF;
           const int vs = jj % ATT_VSTAGES;
-          if (!mbar_wait(&bars->p_full[sb], (jj >> 1) & 1, abort, ATT_WAIT_NS)) return false;
+          if (!mbar_wait(&bars->p_full[sb], (jj / ATT_SBUF) & 1, abort, ATT_WAIT_NS)) return false;
           if (!mbar_wait(&bars->v_full[vs], (jj / ATT_VSTAGES) & 1, abort, ATT_WAIT_NS)) return false;
+          if (jj < 8) BST_TRACE_AT(56 + jj);
           tc_fence_after();
           const uint32_t v_addr = smem_u32(smem + LY::V_OFF + vs * LY::KV_BYTES);
 #pragma unroll
@@ -380,6 +411,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
             mma_ts(tO, tbase + sb * 128 + kk * 8, bdesc, IDESC_PV, (jj > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&bars->o_done);
+          mma_commit(&bars->s_free[sb]);
           mma_commit(&bars->v_empty[vs]);
           return true;
         };
@@ -387,10 +419,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         tc_fence_after();
         for (int j = 0; run && j < T; ++j) {
           const int ks = j % ATT_KSTAGES;
-          const int sb = j & 1;
+          const int sb = j % ATT_SBUF;
           if (!mbar_wait(&bars->k_full[ks], (j / ATT_KSTAGES) & 1, abort, ATT_WAIT_NS)) { run = false; break; }
-          // S buffer sb is free once P_{j-2} V_{j-2} (which read P from it) finished
-          if (j >= 2 && !mbar_wait(&bars->o_done, (j - 2) & 1, abort, ATT_WAIT_NS)) { run = false; break; }
+          if (j < 8) BST_TRACE_AT(40 + j);
+          // S buffer sb is free once P_{j-3} V_{j-3} (which read P from it) finished
+          if (j >= ATT_SBUF && !mbar_wait(&bars->s_free[sb], ((j / ATT_SBUF) - 1) & 1, abort, ATT_WAIT_NS)) {
+            run = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t k_addr = smem_u32(smem + LY::K_OFF + ks * LY::KV_BYTES);
 #pragma unroll
@@ -425,8 +461,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
       }
       const float cs = p.scale_log2;
       for (int j = 0; j < T; ++j) {
-        const int sb = j & 1;
-        if (!warp_wait(&bars->s_full[sb], (j >> 1) & 1, abort)) { ok = false; break; }
+        const int sb = j % ATT_SBUF;
+        if (!warp_wait(&bars->s_full[sb], (j / ATT_SBUF) & 1, abort)) { ok = false; break; }
         tc_fence_after();
         if (tid == 0) BST_TRACE_AT(11 + min(j, 7));
         uint32_t s[ATT_N];
@@ -448,7 +484,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
             for (int c = 0; c < ATT_N; ++c) s[c] = (c < nvalid) ? s[c] : NEG;
           }
         } else {
-          const int tt = j - n_ctx;
+          const int tt = tr0 + j - n_ctx;
           const unsigned long long w0 = (tt == 0) ? mw[0] : mw[2];
           const unsigned long long w1 = (tt == 0) ? mw[1] : mw[3];
 #pragma unroll
@@ -570,10 +606,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   if (p.splits > 1) {
     cluster.sync();
     if (tid == 0) BST_TRACE_AT(29);
+    uint8_t *po = smem + LY::O_OFF;
     switch (p.splits) {
-      case 2: merge_splits<D, 2>(p, cluster, bars, smem + LY::O_OFF, b, kvh, mtile, split, nb); break;
-      case 4: merge_splits<D, 4>(p, cluster, bars, smem + LY::O_OFF, b, kvh, mtile, split, nb); break;
-      default: merge_splits<D, 8>(p, cluster, bars, smem + LY::O_OFF, b, kvh, mtile, split, nb); break;
+      case 2: merge_splits<D, 2>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
+      case 3: merge_splits<D, 3>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
+      case 4: merge_splits<D, 4>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
+      case 5: merge_splits<D, 5>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
+      case 6: merge_splits<D, 6>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
+      case 7: merge_splits<D, 7>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
+      default: merge_splits<D, 8>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
     }
     if (tid == 0) BST_TRACE_AT(30);
     cluster.sync();   // the partials stay readable until every CTA has merged
@@ -611,6 +652,8 @@ __global__ void __launch_bounds__(128) tree_attn_f32_kernel(const float *__restr
                                                             const AttnParamsF32 p) {
   const int h = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   const int nb = p.n[b];
   if (nb < 1 || nb > p.n_max) {
     if (tid == 0 && h == 0 && i == 0) set_err(p.dev_err, BASTION_DEVERR_N);
@@ -743,24 +786,25 @@ AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, i
   const int64_t ctx_tiles = (cap + ATT_N - 1) / ATT_N;
   const int64_t tree_tiles = (n_max + ATT_N - 1) / ATT_N;
   const int64_t units = static_cast<int64_t>(B) * Hkv * pl.mtiles;
-  // KV splits per (b, kvh, M-tile): the power of two up to a portable cluster
-  // of 8 that minimises (waves of resident clusters) x (tiles per CTA + a
-  // fixed cost of about four tiles for set-up, first loads and the merge)
+  const int64_t tot_tiles = ctx_tiles + tree_tiles;
+  // KV splits per (b, kvh, M-tile), up to a portable cluster of 8: the count
+  // that minimises (waves of resident clusters) x (tiles per CTA + a fixed
+  // cost of about four tiles for set-up, first loads and the merge)
   int best = 1;
   double best_cost = 1e30;
-  for (int s = 1; s <= ATT_MAX_SPLITS; s <<= 1) {
-    if (s > 1 && ctx_tiles < 2LL * s) break;
+  for (int s = 1; s <= ATT_MAX_SPLITS; ++s) {
+    if (s > 1 && tot_tiles < 2LL * s) break;
     int per_wave = (s == 1) ? num_sms : max_active_clusters(d, paged, s);
     if (per_wave < 1) continue;
     const int64_t waves = (units + per_wave - 1) / per_wave;
-    const double cost = static_cast<double>(waves) * (4.0 + (ctx_tiles + s - 1) / s + tree_tiles);
+    const double cost = static_cast<double>(waves) * ((s > 1 ? 4.0 : 3.0) + (tot_tiles + s - 1) / s);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;
     }
   }
   pl.splits = best;
-  pl.tiles_per_split = static_cast<int>((ctx_tiles + best - 1) / best);
+  pl.tiles_per_split = static_cast<int>((tot_tiles + best - 1) / best);
   if (pl.tiles_per_split == 0) pl.tiles_per_split = 1;
   pl.ws_bytes = 0;   // the splits merge inside their cluster
   pl.off_o = pl.off_ml = 0;
@@ -775,7 +819,13 @@ cudaError_t prepare_tree_attn() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tree_attn_tc_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnLayout<64>::SMEM);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tree_attn_tc_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnLayout<64>::SMEM);
+  e = cudaFuncSetAttribute(tree_attn_tc_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnLayout<64>::SMEM);
+  if (e != cudaSuccess) return e;
+  if ((e = prefer_max_shared(tree_attn_tc_kernel<128, false>)) != cudaSuccess) return e;
+  if ((e = prefer_max_shared(tree_attn_tc_kernel<128, true>)) != cudaSuccess) return e;
+  if ((e = prefer_max_shared(tree_attn_tc_kernel<64, false>)) != cudaSuccess) return e;
+  if ((e = prefer_max_shared(tree_attn_tc_kernel<64, true>)) != cudaSuccess) return e;
+  return prefer_max_shared(tree_attn_f32_kernel);
 }
 
 cudaError_t launch_tree_attn_tc(const CUtensorMap *maps, const AttnPlan &pl, int B, int n_max, int Hq, int Hkv, int d,
@@ -809,13 +859,9 @@ cudaError_t launch_tree_attn_tc(const CUtensorMap *maps, const AttnPlan &pl, int
   cfg.blockDim = dim3(ATT_THREADS, 1, 1);
   cfg.dynamicSmemBytes = d == 128 ? AttnLayout<128>::SMEM : AttnLayout<64>::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = pl.splits;   // the splits of one (b, kvh, M-tile) form a cluster
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = fill_launch_attrs(attr, 1, pl.splits);   // the splits of one (b, kvh, M-tile) form a cluster
   if (d == 128) {
     if (paged) return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128, true>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
     return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128, false>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
@@ -847,8 +893,14 @@ cudaError_t launch_tree_attn_f32(const float *q, const float *kt, const float *v
   p.mask = reinterpret_cast<const unsigned long long *>(mask);
   p.block_table = block_table;
   p.dev_err = dev_err;
-  tree_attn_f32_kernel<<<dim3(Hq, n_max, B), 128, 0, stream>>>(q, kt, vt, kc, vc, out, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(Hq, n_max, B);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  cfg.attrs = attr;
+  cfg.numAttrs = fill_launch_attrs(attr);
+  return cudaLaunchKernelEx(&cfg, tree_attn_f32_kernel, q, kt, vt, kc, vc, out, p);
 }
 
 }  // namespace bst

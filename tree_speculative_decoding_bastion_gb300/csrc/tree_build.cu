@@ -18,11 +18,9 @@
 // (sortable fp32 log-rho | token | parent) so that one pair of warp max
 // reductions (redux.sync) yields the next node with the exact tie-break
 // (rho desc, token asc, parent asc).  Node state (path sum, depth, next child
-// rank) lives in shared memory together with precomputed "companions" of each
-// node's candidate (its path sum, the parent's next candidate, its own best
-// child), so an insertion is two warp reductions, one broadcast read, and
-// predicated moves in the two owning lanes; the companions of the two new
-// candidates are computed off that dependency chain.  The loop never diverges.  With the controller the pops run in
+// rank) lives in shared memory; per insertion every lane computes the two new
+// keys (the parent's next child, the new node's best child) and the owning
+// lanes take them with predicated moves, so the loop never diverges.  With the controller the pops run in
 // chunks of 32; after each chunk the 32 lanes evaluate rho, A_hat and the
 // S(n+1) < S(n) test in parallel and the first drop ends the tree.
 // Arithmetic is fp32 except single float64 additions for the lse prefix
@@ -54,26 +52,18 @@ struct K2Smem {
   float S32[BASTION_MAX_NODES];        // fp32 logit sum of the path
   float rho[BASTION_MAX_NODES];
   float ahat[BASTION_MAX_NODES];       // ahat[j] = A_hat after nodes 0..j
-  // Companions of node p's current frontier candidate (its child of rank c),
-  // precomputed when the candidate is created so that popping it needs one
-  // broadcast read: the candidate's path sum, node p's next candidate (rank
-  // c + 1: key and path sum) and the candidate's own best child (key without
-  // the parent byte, which is the candidate's future index, and path sum).
-  float cs[BASTION_MAX_NODES];
-  unsigned long long nk[BASTION_MAX_NODES];
-  float ns[BASTION_MAX_NODES];
-  unsigned long long fk[BASTION_MAX_NODES];
-  float fs[BASTION_MAX_NODES];
   int n_final;
 };
 
-// Ordering key of a candidate at depth d (>= 1) with path logit sum S, token
-// tok and parent index par: high word sortable fp32 log rho (rho desc), low word
-// (0x3FFFF - tok) << 8 | (255 - par) (token asc, then parent asc).
-BST_DEV unsigned long long key_of(const K2Smem &sm, float S, int d, int tok, int par) {
-  const float key = (S - sm.Phi[d]) - sm.Plo[d];
-  const uint32_t lo = ((0x3FFFFu - static_cast<uint32_t>(tok)) << 8) | (255u - static_cast<uint32_t>(par));
-  return (static_cast<unsigned long long>(sortable(key)) << 32) | lo;
+// Frontier key of "child of rank c of node `node` at depth d_node":
+// high word sortable fp32 log rho (rho desc), low word (0x3FFFF - token) << 8 |
+// (255 - parent) (token asc, then parent asc).  0 means "no candidate".
+BST_DEV uint64_t cand_key(const K2Smem &sm, int k, int node, float S_node, int d_node, int c) {
+  const float S = S_node + sm.lg[d_node * k + c];                    // position d_node + 1
+  const float key = (S - sm.Phi[d_node + 1]) - sm.Plo[d_node + 1];   // log rho, fp32
+  const uint32_t lo = ((0x3FFFFu - static_cast<uint32_t>(sm.ids[d_node * k + c])) << 8) |
+                      (255u - static_cast<uint32_t>(node));
+  return (static_cast<uint64_t>(sortable(key)) << 32) | lo;
 }
 
 template <int SLOTS>
@@ -92,6 +82,9 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
   const bool controller = (Ctab != nullptr);
 
   if (tid == 0) BST_STAMP(g_k2_trace, 0);
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 0) BST_STAMP(g_k2_trace, 4);
   // ---- load the request's candidate table
   for (int e = tid; e < K * k; e += K2_THREADS) {
     int32_t id = ids_g[static_cast<int64_t>(b) * K * k + e];
@@ -139,24 +132,11 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
   // stream: both new frontier keys are computed by all lanes, and the two
   // owning lanes take them with predicated moves.
   if (tid < 32) {
-    unsigned long long slot[SLOTS];
+    uint64_t slot[SLOTS];
 #pragma unroll
     for (int r = 0; r < SLOTS; ++r) slot[r] = 0ull;
-    // the root's frontier candidate (rank 0 of position 1) and its companions
-    {
-      const float s0 = sm.lg[0];
-      const unsigned long long k0 = key_of(sm, s0, 1, sm.ids[0], 0);
-      if (lane == 0) {
-        slot[0] = k0;
-        sm.cs[0] = s0;
-        sm.nk[0] = (k > 1) ? key_of(sm, sm.lg[1], 1, sm.ids[1], 0) : 0ull;
-        sm.ns[0] = (k > 1) ? sm.lg[1] : 0.f;
-        sm.fk[0] = (K > 1) ? key_of(sm, s0 + sm.lg[k], 2, sm.ids[k], 255) : 0ull;
-        sm.fs[0] = (K > 1) ? s0 + sm.lg[k] : 0.f;
-      }
-      __syncwarp();
-    }
-    unsigned long long best = slot[0];
+    if (lane == 0) slot[0] = cand_key(sm, k, 0, 0.f, 0, 0);
+    uint64_t best = slot[0];
 
     int n = 1;
     int n_final = -1;
@@ -175,14 +155,21 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
         const int p = 255 - static_cast<int>(ml & 0xFFu);
         const int tokn = 0x3FFFF - static_cast<int>(ml >> 8);
         const int t = n;
-        // everything the pop needs was precomputed for node p's candidate
         const int dcp = sm.dc[p];
-        const float St = sm.cs[p];
-        const unsigned long long kP = sm.nk[p];
-        const float SP = sm.ns[p];
-        const unsigned long long fkp = sm.fk[p];
-        const float ST = sm.fs[p];
-        const unsigned long long kT = fkp ? (fkp | static_cast<unsigned long long>(255u - static_cast<uint32_t>(t))) : 0ull;
+        const int dp = dcp & 0xFF;
+        const int c = dcp >> 8;
+        const float Sp = sm.S32[p];
+        const float St = Sp + sm.lg[dp * k + c];   // the same sum the popped key was made from
+        const int dt = dp + 1;
+        const uint64_t kP = (c + 1 < k) ? cand_key(sm, k, p, Sp, dp, c + 1) : 0ull;   // p's next child
+        const uint64_t kT = (dt < K) ? cand_key(sm, k, t, St, dt, 0) : 0ull;         // t's best child
+        if (lane == 0) {
+          sm.par[t] = p;
+          sm.tok[t] = tokn;
+          sm.dc[t] = dt;
+          sm.S32[t] = St;
+          sm.dc[p] = dcp + 256;
+        }
         const bool ownP = lane == (p & 31);
         const bool ownT = lane == (t & 31);
         const int rp = p >> 5, rt = t >> 5;
@@ -192,47 +179,6 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
           if (ownP && r == rp) slot[r] = kP;
           if (ownT && r == rt) slot[r] = kT;
           best = slot[r] > best ? slot[r] : best;
-        }
-        // companions of the two new candidates: node p's rank c+1 child and
-        // node t's rank 0 child (off the reduction's dependency chain)
-        const int dp = dcp & 0xFF;
-        const int c = dcp >> 8;
-        const int dt = dp + 1;
-        const float Sp = sm.S32[p];
-        unsigned long long nkp = 0ull, fkp2 = 0ull, nkt = 0ull, fkt = 0ull;
-        float nsp = 0.f, fsp = 0.f, nst = 0.f, fst = 0.f;
-        if (c + 2 < k) {   // node p's rank c+2 child
-          nsp = Sp + sm.lg[dp * k + c + 2];
-          nkp = key_of(sm, nsp, dt, sm.ids[dp * k + c + 2], p);
-        }
-        if (dt < K) {      // best child of node p's rank c+1 child (parent byte added when it is popped)
-          fsp = SP + sm.lg[dt * k];
-          fkp2 = key_of(sm, fsp, dt + 1, sm.ids[dt * k], 255);
-        }
-        if (dt < K && 1 < k) {   // node t's rank 1 child
-          nst = St + sm.lg[dt * k + 1];
-          nkt = key_of(sm, nst, dt + 1, sm.ids[dt * k + 1], t);
-        }
-        if (dt + 1 < K) {  // best child of node t's rank 0 child
-          fst = ST + sm.lg[(dt + 1) * k];
-          fkt = key_of(sm, fst, dt + 2, sm.ids[(dt + 1) * k], 255);
-        }
-        if (lane == 0) {
-          sm.par[t] = p;
-          sm.tok[t] = tokn;
-          sm.dc[t] = dt;
-          sm.S32[t] = St;
-          sm.dc[p] = dcp + 256;
-          sm.cs[p] = SP;
-          sm.nk[p] = nkp;
-          sm.ns[p] = nsp;
-          sm.fk[p] = fkp2;
-          sm.fs[p] = fsp;
-          sm.cs[t] = ST;
-          sm.nk[t] = nkt;
-          sm.ns[t] = nst;
-          sm.fk[t] = fkt;
-          sm.fs[t] = fst;
         }
         ++n;
         __syncwarp();
@@ -362,17 +308,24 @@ cudaError_t launch_tree_build(const int32_t *ids, const float *lg, const double 
                               int32_t *depth, int32_t *pos, float *rho, uint64_t *mask, float *ahat, float *S,
                               float *S_curve, uint32_t *dev_err, cudaStream_t stream) {
   auto *m = reinterpret_cast<unsigned long long *>(mask);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B, 1, 1);
+  cfg.blockDim = dim3(K2_THREADS, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  cfg.attrs = attr;
+  cfg.numAttrs = fill_launch_attrs(attr);
   // frontier slots per lane: one per 32 nodes of the budget
-  if (n_max <= 64)
-    tree_build_kernel<2><<<B, K2_THREADS, 0, stream>>>(ids, lg, lse, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR,
-                                                       n, parent, token, depth, pos, rho, m, ahat, S, S_curve, dev_err);
-  else if (n_max <= 128)
-    tree_build_kernel<4><<<B, K2_THREADS, 0, stream>>>(ids, lg, lse, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR,
-                                                       n, parent, token, depth, pos, rho, m, ahat, S, S_curve, dev_err);
-  else
-    tree_build_kernel<8><<<B, K2_THREADS, 0, stream>>>(ids, lg, lse, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR,
-                                                       n, parent, token, depth, pos, rho, m, ahat, S, S_curve, dev_err);
-  return cudaGetLastError();
+  auto *fn = n_max <= 64 ? tree_build_kernel<2> : n_max <= 128 ? tree_build_kernel<4> : tree_build_kernel<8>;
+  return cudaLaunchKernelEx(&cfg, fn, ids, lg, lse, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR, n, parent,
+                            token, depth, pos, rho, m, ahat, S, S_curve, dev_err);
+}
+
+cudaError_t prepare_tree_build() {
+  cudaError_t e;
+  if ((e = prefer_max_shared(tree_build_kernel<2>)) != cudaSuccess) return e;
+  if ((e = prefer_max_shared(tree_build_kernel<4>)) != cudaSuccess) return e;
+  return prefer_max_shared(tree_build_kernel<8>);
 }
 
 }  // namespace bst
