@@ -42,7 +42,7 @@ constexpr int K1_THREADS = 512;   // 4 warps per scheduler hide the MUFU / share
 constexpr int K1_WARPS = K1_THREADS / 32;
 constexpr int K1_CAP = 1024;                      // candidate buffer
 constexpr int K1_MAXC = 8;                        // CTAs per cluster (row), portable
-constexpr int K1_CHUNK_BYTES = 48 * 1024;         // preferred staged bytes per CTA
+constexpr int K1_CHUNK_BYTES = 38 * 1024;         // preferred staged bytes per CTA (8 CTAs for a 152K bf16 row)
 constexpr int K1_MAX_SMEM = 200 * 1024;           // largest chunk (very long rows)
 constexpr uint64_t K1_WAIT_NS = 200ull * 1000ull * 1000ull;
 

@@ -13,20 +13,22 @@
 // split).  The M rows pack g = Hq/Hkv query heads x tree nodes of one KV head
 // (GQA), so every K/V tile is used by all heads of its group.  Roles:
 //   warp 4      TMA producer: Q once, then K tiles (128 keys, 3-stage ring,
-//               running one tile ahead) and V tiles (2-stage ring), 128-byte
+//               running one tile ahead) and V tiles (3-stage ring), 128-byte
 //               swizzle; paged caches are gathered page by page through a 4-D
 //               tensor map; no multicast.
-//   warp 5      MMA issuer (one thread): S = Q K^T into TMEM (two S buffers),
-//               O += P V with P read from TMEM (P aliases its S buffer).
+//   warp 5      MMA issuer (one thread): S = Q K^T into TMEM (three S
+//               buffers, each freed by its own barrier once the P V that
+//               read it finished), O += P V with P read from TMEM (P aliases
+//               its S buffer).
 //   warps 0-3   softmax: thread r owns TMEM lane r = M-tile row r; it reads S,
 //               applies the context bound or the ancestor bits, keeps the
 //               running max / sum in the log2 domain, writes P (bf16) to TMEM,
 //               and rescales O only when its row max grew by more than 2^8
 //               (the exact result is the same for any running reference max).
-// The KV splits of one (b, kvh, M-tile) form one thread-block cluster: each CTA
-// leaves its partial (O, m, l) in its own shared memory and, after a cluster
-// barrier, every CTA merges a slice of the rows by reading the others' partials
-// over distributed shared memory.  No workspace, no global partials.
+// A request's context tiles followed by its tree tiles are spread evenly over
+// the KV splits.  The splits of one (b, kvh, M-tile) form one thread-block
+// cluster: each CTA stores its partial (O, m, l) to the workspace in L2, one
+// cluster barrier publishes them, and every CTA merges a slice of the rows.
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // BASTION_DEVERR_TIMEOUT, drains what it issued and frees its TMEM.
 //
@@ -66,6 +68,7 @@ struct AttnParams {
   const unsigned long long *mask;
   const int32_t *block_table;
   uint16_t *out;             // bf16 [B, n_max, Hq, d]
+  float4 *part;              // split partials (workspace), used when splits > 1
   uint32_t *dev_err;
 };
 
@@ -82,8 +85,6 @@ struct AttnBars {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  float part_m[ATT_M];       // this CTA's partial row max (log2 domain)
-  float part_l[ATT_M];       // and row sum, for the cluster merge
 };
 
 template <int D>
@@ -95,10 +96,7 @@ struct AttnLayout {
   static constexpr int K_OFF = Q_BYTES;
   static constexpr int V_OFF = K_OFF + ATT_KSTAGES * KV_BYTES;
   static constexpr int BAR_OFF = V_OFF + ATT_VSTAGES * KV_BYTES;
-  // the partial O (128 rows x D fp32, stored as [D/4][128] float4) reuses the
-  // K ring once every MMA has finished
-  static constexpr int O_OFF = K_OFF;
-  static_assert(ATT_M * D * 4 <= ATT_KSTAGES * KV_BYTES, "partial O must fit the K ring");
+
   static constexpr int USED = BAR_OFF + static_cast<int>(sizeof(AttnBars));
   // 1024 bytes of slack for aligning the dynamic shared memory base; at least
   // 120 KB so that a single CTA owns each SM (its TMEM allocation is 512 columns).
@@ -146,44 +144,50 @@ BST_DEV float ex2(float x) {
   return y;
 }
 
-// Merge of the S split partials for the rows this CTA owns: rows
-// [split * 128/S, (split + 1) * 128/S), each of the 128 threads one row and D/S
-// columns.  Every remote load is issued before any is used.
+// KV-split partials live in the workspace, one slot per (b, kvh, M-tile,
+// split): (D/4 + 1) x 128 float4, column-major by float4 (chunk c of row r at
+// c * 128 + r, so a warp's store or load of one chunk is 512 contiguous
+// bytes); the last chunk of a row holds (m, l, 0, 0) with m in the log2 domain.
+template <int D>
+BST_DEV float4 *part_slot(const AttnParams &p, int b, int kvh, int mtile, int split) {
+  const int64_t slot = ((static_cast<int64_t>(b) * p.Hkv + kvh) * p.mtiles + mtile) * p.splits + split;
+  return p.part + slot * (D / 4 + 1) * ATT_M;
+}
+
+// Merge of the S split partials (every CTA of the cluster, after a cluster
+// barrier that follows all main loops and partial stores).  CTA `split` owns
+// R = ceil(128 / S) rows of the M-tile: O = sum_s 2^(m_s - M) O_s /
+// sum_s 2^(m_s - M) l_s.  G threads share a row, each taking CPG of its D/4
+// float4 columns; every load is issued before any is used (one L2 round trip).
 template <int D, int S>
-BST_DEV void merge_splits(const AttnParams &p, cg::cluster_group &cluster, AttnBars *bars, uint8_t *part_o, int b,
-                          int kvh, int mtile, int split, int nb) {
-  // this CTA merges R rows with all of its threads: G threads share a row,
-  // each taking CPG of the row's D/4 float4 columns (consecutive threads take
-  // consecutive rows, so the partials are read without bank conflicts).  All
-  // remote loads are issued before any of them is used: one round trip.
+BST_DEV void merge_splits(const AttnParams &p, int b, int kvh, int mtile, int split, int nb) {
   constexpr int R = (ATT_M + S - 1) / S;
   constexpr int G = ATT_THREADS / R;
   constexpr int NC4 = D / 4;
   constexpr int CPG = (NC4 + G - 1) / G;
   const int tid = threadIdx.x;
   if (tid >= R * G) return;
-  const int rr = split * R + (tid % R);
+  const int rl = tid % R;
+  const int rr = split * R + rl;
   if (rr >= ATT_M) return;
   const int g = tid / R;
   const int c40 = g * CPG;
   const int prow = mtile * ATT_M + rr;
   const int nd = prow / p.g;
   if (nd >= nb) return;
-  float ms[S], ls[S];
+  float4 ml[S];
   float4 ov[S][CPG];
 #pragma unroll
   for (int s2 = 0; s2 < S; ++s2) {
-    const AttnBars *ob = cluster.map_shared_rank(bars, s2);
-    ms[s2] = ob->part_m[rr];
-    ls[s2] = ob->part_l[rr];
-    const float4 *src = cluster.map_shared_rank(reinterpret_cast<const float4 *>(part_o), s2);
+    const float4 *src = part_slot<D>(p, b, kvh, mtile, s2);
+    ml[s2] = __ldcg(src + NC4 * ATT_M + rr);
 #pragma unroll
     for (int c = 0; c < CPG; ++c)
-      ov[s2][c] = (c40 + c < NC4) ? src[(c40 + c) * ATT_M + rr] : make_float4(0.f, 0.f, 0.f, 0.f);
+      ov[s2][c] = (c40 + c < NC4) ? __ldcg(src + (c40 + c) * ATT_M + rr) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float M = -CUDART_INF_F;
 #pragma unroll
-  for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, ms[s2]);
+  for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, ml[s2].x);
   float4 acc[CPG];
 #pragma unroll
   for (int c = 0; c < CPG; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -191,8 +195,8 @@ BST_DEV void merge_splits(const AttnParams &p, cg::cluster_group &cluster, AttnB
 #pragma unroll
   for (int s2 = 0; s2 < S; ++s2) {
     // empty splits carry m = -inf, l = 0 and a zero O
-    const float w = (ms[s2] == -CUDART_INF_F) ? 0.f : ex2(ms[s2] - M);
-    lsum += w * ls[s2];
+    const float w = (ml[s2].x == -CUDART_INF_F) ? 0.f : ex2(ml[s2].x - M);
+    lsum += w * ml[s2].y;
 #pragma unroll
     for (int c = 0; c < CPG; ++c) {
       acc[c].x += w * ov[s2][c].x;
@@ -576,23 +580,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
           }
         }
       } else {
-        // partial for the cluster merge: O as [D/4][128 rows] float4 (each
-        // warp writes 512 contiguous bytes per column group), m and l per row
-        float4 *sO = reinterpret_cast<float4 *>(smem + LY::O_OFF);
+        // this split's partial for the merge
+        float4 *dp = part_slot<D>(p, b, kvh, mtile, split);
 #pragma unroll
-        for (int c = 0; c < D; c += 4) sO[(c >> 2) * ATT_M + r] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-        bars->part_m[r] = ok ? m_run : -CUDART_INF_F;
-        bars->part_l[r] = ok ? l_run : 0.f;
+        for (int c = 0; c < D; c += 4) dp[(c >> 2) * ATT_M + r] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        dp[(D / 4) * ATT_M + r] = make_float4(ok ? m_run : -CUDART_INF_F, ok ? l_run : 0.f, 0.f, 0.f);
       }
       if (tid == 0) BST_TRACE_AT(28);
     }
   } else if (p.splits > 1 && tid < 128) {
     // nothing to attend to in this split: an empty (zero) partial
-    float4 *sO = reinterpret_cast<float4 *>(smem + LY::O_OFF);
+    float4 *dp = part_slot<D>(p, b, kvh, mtile, split);
 #pragma unroll
-    for (int c = 0; c < D; c += 4) sO[(c >> 2) * ATT_M + r] = make_float4(0.f, 0.f, 0.f, 0.f);
-    bars->part_m[r] = -CUDART_INF_F;
-    bars->part_l[r] = 0.f;
+    for (int c = 0; c < D; c += 4) dp[(c >> 2) * ATT_M + r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    dp[(D / 4) * ATT_M + r] = make_float4(-CUDART_INF_F, 0.f, 0.f, 0.f);
   }
 
   // all roles are done with TMEM
@@ -602,22 +603,21 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   if (T > 0 && warp == 0) tmem_dealloc(tbase, 512);
   if (T > 0 && *abort && tid == 0) set_err(p.dev_err, BASTION_DEVERR_TIMEOUT);
 
-  // ---- cluster merge of the splits over distributed shared memory
+  // ---- merge of the KV splits: the cluster barrier (release / acquire)
+  // publishes every split's partial, then each CTA merges its rows from L2
   if (p.splits > 1) {
     cluster.sync();
     if (tid == 0) BST_TRACE_AT(29);
-    uint8_t *po = smem + LY::O_OFF;
     switch (p.splits) {
-      case 2: merge_splits<D, 2>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
-      case 3: merge_splits<D, 3>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
-      case 4: merge_splits<D, 4>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
-      case 5: merge_splits<D, 5>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
-      case 6: merge_splits<D, 6>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
-      case 7: merge_splits<D, 7>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
-      default: merge_splits<D, 8>(p, cluster, bars, po, b, kvh, mtile, split, nb); break;
+      case 2: merge_splits<D, 2>(p, b, kvh, mtile, split, nb); break;
+      case 3: merge_splits<D, 3>(p, b, kvh, mtile, split, nb); break;
+      case 4: merge_splits<D, 4>(p, b, kvh, mtile, split, nb); break;
+      case 5: merge_splits<D, 5>(p, b, kvh, mtile, split, nb); break;
+      case 6: merge_splits<D, 6>(p, b, kvh, mtile, split, nb); break;
+      case 7: merge_splits<D, 7>(p, b, kvh, mtile, split, nb); break;
+      default: merge_splits<D, 8>(p, b, kvh, mtile, split, nb); break;
     }
     if (tid == 0) BST_TRACE_AT(30);
-    cluster.sync();   // the partials stay readable until every CTA has merged
   }
   if (tid == 0) BST_TRACE_AT(31);
 }
@@ -806,7 +806,8 @@ AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, i
   pl.splits = best;
   pl.tiles_per_split = static_cast<int>((tot_tiles + best - 1) / best);
   if (pl.tiles_per_split == 0) pl.tiles_per_split = 1;
-  pl.ws_bytes = 0;   // the splits merge inside their cluster
+  // one partial slot per (b, kvh, M-tile, split) when the KV is split
+  pl.ws_bytes = best > 1 ? static_cast<size_t>(units) * best * (d / 4 + 1) * ATT_M * sizeof(float4) : 0;
   pl.off_o = pl.off_ml = 0;
   return pl;
 }
@@ -833,8 +834,8 @@ cudaError_t launch_tree_attn_tc(const CUtensorMap *maps, const AttnPlan &pl, int
                                 const int32_t *ctx_len, const int32_t *n, const uint64_t *mask,
                                 const int32_t *block_table, void *out, void *ws, uint32_t *dev_err,
                                 cudaStream_t stream) {
-  (void)ws;
   AttnParams p{};
+  p.part = reinterpret_cast<float4 *>(ws);
   p.B = B;
   p.n_max = n_max;
   p.Hq = Hq;

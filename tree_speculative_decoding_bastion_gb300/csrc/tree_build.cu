@@ -17,11 +17,15 @@
 // frontier: node i lives in lane i % 32, register slot i / 32, as a 64-bit key
 // (sortable fp32 log-rho | token | parent) so that one pair of warp max
 // reductions (redux.sync) yields the next node with the exact tie-break
-// (rho desc, token asc, parent asc).  Node state (path sum, depth, next child
-// rank) lives in shared memory; per insertion every lane computes the two new
-// keys (the parent's next child, the new node's best child) and the owning
-// lanes take them with predicated moves, so the loop never diverges.  With the controller the pops run in
-// chunks of 32; after each chunk the 32 lanes evaluate rho, A_hat and the
+// (rho desc, token asc, parent asc).  The candidate table is packed as
+// {logit, token word} pairs, the lse prefix as {hi, lo} float pairs and the
+// node state as {path sum, depth | next rank}, so a pop reads everything it
+// needs with five 64-bit shared loads.  Every lane computes the two new keys
+// (the parent's next child, the new node's best child), the owning lanes take
+// them with predicated moves, and every lane writes the same node state, so
+// the loop has no divergent branch and no warp barrier.  With the controller
+// the pops run until the stop rule can first apply (n_min + 1 nodes) and then
+// in chunks of 8; after each chunk the lanes evaluate rho, A_hat and the
 // S(n+1) < S(n) test in parallel and the first drop ends the tree.
 // Arithmetic is fp32 except single float64 additions for the lse prefix
 // (this GPU's FP64 pipe is narrow, so no float64 exp/log/division).
@@ -41,29 +45,22 @@ extern "C" cudaError_t bastion_trace_read_tree(void *dst, size_t bytes) {
 constexpr int K2_THREADS = 256;
 
 struct K2Smem {
-  int32_t ids[BASTION_MAX_DEPTH * BASTION_MAX_TOPK];   // [K][k]
-  float lg[BASTION_MAX_DEPTH * BASTION_MAX_TOPK];
+  uint2 E[BASTION_MAX_DEPTH * BASTION_MAX_TOPK];   // [K][k]: {logit bits, (0x3FFFF - token) << 8}
   double P64[BASTION_MAX_DEPTH + 1];   // sum of lse over positions 1..d
-  float Phi[BASTION_MAX_DEPTH + 1];    // P64 as a float pair (hi + lo)
-  float Plo[BASTION_MAX_DEPTH + 1];
-  int32_t par[BASTION_MAX_NODES];
-  int32_t tok[BASTION_MAX_NODES];
-  int32_t dc[BASTION_MAX_NODES];       // depth | (rank of the next child to offer << 8)
-  float S32[BASTION_MAX_NODES];        // fp32 logit sum of the path
+  float2 PP[BASTION_MAX_DEPTH + 2];    // P64 as a float pair (hi, lo); one spare entry
+  uint2 NS[BASTION_MAX_NODES];         // {fp32 logit sum of the path (bits), depth | next rank << 8}
+  int2 PT[BASTION_MAX_NODES];          // {parent, token}
   float rho[BASTION_MAX_NODES];
   float ahat[BASTION_MAX_NODES];       // ahat[j] = A_hat after nodes 0..j
   int n_final;
 };
 
-// Frontier key of "child of rank c of node `node` at depth d_node":
-// high word sortable fp32 log rho (rho desc), low word (0x3FFFF - token) << 8 |
-// (255 - parent) (token asc, then parent asc).  0 means "no candidate".
-BST_DEV uint64_t cand_key(const K2Smem &sm, int k, int node, float S_node, int d_node, int c) {
-  const float S = S_node + sm.lg[d_node * k + c];                    // position d_node + 1
-  const float key = (S - sm.Phi[d_node + 1]) - sm.Plo[d_node + 1];   // log rho, fp32
-  const uint32_t lo = ((0x3FFFFu - static_cast<uint32_t>(sm.ids[d_node * k + c])) << 8) |
-                      (255u - static_cast<uint32_t>(node));
-  return (static_cast<uint64_t>(sortable(key)) << 32) | lo;
+// Frontier key of a candidate with path sum S, table entry e = {logit, token
+// word} at key depth d (PP[d]) and parent byte parb = 255 - parent: high word
+// sortable fp32 log rho (rho desc), low word (0x3FFFF - token) << 8 | parb.
+BST_DEV uint64_t cand_key2(float S, float2 pp, uint32_t tokw, uint32_t parb) {
+  const float key = (S - pp.x) - pp.y;   // log rho, fp32
+  return (static_cast<uint64_t>(sortable(key)) << 32) | tokw | parb;
 }
 
 template <int SLOTS>
@@ -92,8 +89,8 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
       set_err(dev_err, BASTION_DEVERR_TOKEN);
       id = 0;
     }
-    sm.ids[e] = id;
-    sm.lg[e] = lg_g[static_cast<int64_t>(b) * K * k + e];
+    sm.E[e] = make_uint2(__float_as_uint(lg_g[static_cast<int64_t>(b) * K * k + e]),
+                         (0x3FFFFu - static_cast<uint32_t>(id)) << 8);
   }
   if (tid < 32) {
     // prefix of the positions' lse (warp scan; K <= 32), kept in float64 and as
@@ -107,20 +104,17 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
     if (tid < K) {
       sm.P64[tid + 1] = P;
       const float hi = static_cast<float>(P);
-      sm.Phi[tid + 1] = hi;
-      sm.Plo[tid + 1] = static_cast<float>(P - static_cast<double>(hi));
+      sm.PP[tid + 1] = make_float2(hi, static_cast<float>(P - static_cast<double>(hi)));
     }
   }
   if (tid == 0) {
     sm.P64[0] = 0.0;
-    sm.Phi[0] = 0.f;
-    sm.Plo[0] = 0.f;
+    sm.PP[0] = make_float2(0.f, 0.f);
+    sm.PP[K + 1] = make_float2(0.f, 0.f);
     int32_t rt = root_tok[b];
     if (rt < 0 || rt >= V) set_err(dev_err, BASTION_DEVERR_TOKEN);
-    sm.par[0] = -1;
-    sm.tok[0] = rt;
-    sm.dc[0] = 0;
-    sm.S32[0] = 0.f;
+    sm.PT[0] = make_int2(-1, rt);
+    sm.NS[0] = make_uint2(__float_as_uint(0.f), 0u);
     sm.rho[0] = 1.f;
     sm.ahat[0] = 1.f;
     sm.n_final = 1;
@@ -135,14 +129,16 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
     uint64_t slot[SLOTS];
 #pragma unroll
     for (int r = 0; r < SLOTS; ++r) slot[r] = 0ull;
-    if (lane == 0) slot[0] = cand_key(sm, k, 0, 0.f, 0, 0);
+    if (lane == 0) slot[0] = cand_key2(__uint_as_float(sm.E[0].x), sm.PP[1], sm.E[0].y, 255u);
     uint64_t best = slot[0];
 
     int n = 1;
     int n_final = -1;
     int chunk_start = 1;
     while (n_final < 0) {
-      const int target = controller ? min(n_max, n + 32) : n_max;
+      // with the controller, pop until the stop rule can first apply
+      // (n_min + 1 nodes), then test it every 8 pops
+      const int target = controller ? min(n_max, max(n + 8, n_min + 1)) : n_max;
       bool exhausted = false;
       while (n < target) {
         const uint32_t bh = static_cast<uint32_t>(best >> 32);
@@ -155,64 +151,69 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
         const int p = 255 - static_cast<int>(ml & 0xFFu);
         const int tokn = 0x3FFFF - static_cast<int>(ml >> 8);
         const int t = n;
-        const int dcp = sm.dc[p];
+        const uint2 ns = sm.NS[p];
+        const float Sp = __uint_as_float(ns.x);
+        const int dcp = static_cast<int>(ns.y);
         const int dp = dcp & 0xFF;
         const int c = dcp >> 8;
-        const float Sp = sm.S32[p];
-        const float St = Sp + sm.lg[dp * k + c];   // the same sum the popped key was made from
         const int dt = dp + 1;
-        const uint64_t kP = (c + 1 < k) ? cand_key(sm, k, p, Sp, dp, c + 1) : 0ull;   // p's next child
-        const uint64_t kT = (dt < K) ? cand_key(sm, k, t, St, dt, 0) : 0ull;         // t's best child
-        if (lane == 0) {
-          sm.par[t] = p;
-          sm.tok[t] = tokn;
-          sm.dc[t] = dt;
-          sm.S32[t] = St;
-          sm.dc[p] = dcp + 256;
-        }
-        const bool ownP = lane == (p & 31);
-        const bool ownT = lane == (t & 31);
-        const int rp = p >> 5, rt = t >> 5;
+        const int base = dp * k + c;
+        const bool vP = c + 1 < k;    // node p has a next child
+        const bool vT = dt < K;       // the new node has children
+        const uint2 e0 = sm.E[base];                  // the popped candidate
+        const uint2 e1 = sm.E[vP ? base + 1 : 0];     // p's next child
+        const uint2 f0 = sm.E[vT ? dt * k : 0];       // t's best child
+        const float2 pp1 = sm.PP[dt];
+        const float2 pp2 = sm.PP[dt + 1];
+        const float St = Sp + __uint_as_float(e0.x);   // the same sum the popped key was made from
+        const uint64_t kP = vP ? cand_key2(Sp + __uint_as_float(e1.x), pp1, e1.y, 255u - static_cast<uint32_t>(p)) : 0ull;
+        const uint64_t kT = vT ? cand_key2(St + __uint_as_float(f0.x), pp2, f0.y, 255u - static_cast<uint32_t>(t)) : 0ull;
+        // every lane stores the same values (no divergent branch); each lane
+        // then reads back its own writes, so the loop needs no warp barrier
+        sm.NS[t] = make_uint2(__float_as_uint(St), static_cast<uint32_t>(dt));
+        sm.NS[p].y = static_cast<uint32_t>(dcp + 256);
+        sm.PT[t] = make_int2(p, tokn);
         best = 0ull;
 #pragma unroll
         for (int r = 0; r < SLOTS; ++r) {
-          if (ownP && r == rp) slot[r] = kP;
-          if (ownT && r == rt) slot[r] = kT;
+          const int me = r * 32 + lane;
+          slot[r] = (me == p) ? kP : slot[r];
+          slot[r] = (me == t) ? kT : slot[r];
           best = slot[r] > best ? slot[r] : best;
         }
         ++n;
-        __syncwarp();
       }
+      __syncwarp();
       if (controller) {
-        // rho, A_hat and the stop test for the nodes of this chunk
-        const int j = chunk_start + lane;
-        float r = 0.f;
-        if (j < n) {
-          const float key = static_cast<float>(static_cast<double>(sm.S32[j]) - sm.P64[sm.dc[j] & 0xFF]);
-          r = expf(key);
-          sm.rho[j] = r;
-        }
-        // inclusive prefix sum over the lanes
+        // rho, A_hat and the stop test for the nodes of this chunk, 32 at a time
+        for (int cs = chunk_start; cs < n && n_final < 0; cs += 32) {
+          const int j = cs + lane;
+          float r = 0.f;
+          if (j < n) {
+            const uint2 nj = sm.NS[j];
+            const float key = static_cast<float>(static_cast<double>(__uint_as_float(nj.x)) - sm.P64[nj.y & 0xFF]);
+            r = expf(key);
+            sm.rho[j] = r;
+          }
+          // inclusive prefix sum over the lanes
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(FULL, r, o);
-          if (lane >= o) r += y;
+          for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(FULL, r, o);
+            if (lane >= o) r += y;
+          }
+          const float base = sm.ahat[cs - 1];
+          const float a_next = base + r;                  // A_hat(j + 1)
+          float a_prev = __shfl_up_sync(FULL, a_next, 1);
+          if (lane == 0) a_prev = base;                   // A_hat(j)
+          if (j < n) sm.ahat[j] = a_next;
+          // tree of size j grows to j + 1 only if S(j + 1) >= S(j)
+          const bool drop = (j < n) && (j >= n_min) && (a_next * Ctab[j] < a_prev * Ctab[j + 1]);
+          const unsigned dm = __ballot_sync(FULL, drop);
+          if (dm) n_final = cs + (__ffs(dm) - 1);
+          __syncwarp();
         }
-        const float base = sm.ahat[chunk_start - 1];
-        const float a_next = base + r;                  // A_hat(j + 1)
-        float a_prev = __shfl_up_sync(FULL, a_next, 1);
-        if (lane == 0) a_prev = base;                   // A_hat(j)
-        if (j < n) sm.ahat[j] = a_next;
-        // tree of size j grows to j + 1 only if S(j + 1) >= S(j)
-        const bool drop = (j < n) && (j >= n_min) && (a_next * Ctab[j] < a_prev * Ctab[j + 1]);
-        const unsigned dm = __ballot_sync(FULL, drop);
-        if (dm) {
-          n_final = chunk_start + (__ffs(dm) - 1);
-        } else if (exhausted || n >= n_max) {
-          n_final = n;
-        }
+        if (n_final < 0 && (exhausted || n >= n_max)) n_final = n;
         chunk_start = n;
-        __syncwarp();
       } else {
         n_final = n;
       }
@@ -226,7 +227,8 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
   // ---- rho and A_hat for a fixed budget (the controller filled them already)
   if (!controller) {
     for (int j = 1 + tid; j < nf; j += K2_THREADS) {
-      const float key = static_cast<float>(static_cast<double>(sm.S32[j]) - sm.P64[sm.dc[j] & 0xFF]);
+      const uint2 nj = sm.NS[j];
+      const float key = static_cast<float>(static_cast<double>(__uint_as_float(nj.x)) - sm.P64[nj.y & 0xFF]);
       sm.rho[j] = expf(key);
     }
     __syncthreads();
@@ -256,10 +258,12 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
   for (int i = tid; i < n_max; i += K2_THREADS) {
     const int64_t o = row0 + i;
     if (i < nf) {
-      parent[o] = sm.par[i];
-      token[o] = sm.tok[i];
-      depth[o] = sm.dc[i] & 0xFF;
-      pos[o] = cl + (sm.dc[i] & 0xFF);
+      const int2 pt = sm.PT[i];
+      const int di = static_cast<int>(sm.NS[i].y & 0xFFu);
+      parent[o] = pt.x;
+      token[o] = pt.y;
+      depth[o] = di;
+      pos[o] = cl + di;
       rho_out[o] = sm.rho[i];
       if (S_curve) {
         const float c = controller ? Ctab[i + 1] : 1.f;
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
         else if (w == 1) m1 |= bit;
         else if (w == 2) m2 |= bit;
         else m3 |= bit;
-        j = sm.par[j];
+        j = sm.PT[j].x;
       }
       unsigned long long *mrow = mask + o * W;
       mrow[0] = m0;
