@@ -36,15 +36,20 @@ from tree_speculative_decoding_bastion_gb300 import inputs as I  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 DEFAULT_WORKLOAD = "qwen3_8b_b1"
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from an
-# ncu capture of the default workload (summaries in profiles/), valid only
-# while the kernel's sources hash to the value they had at capture time.
-KNOWN_TRAFFIC = {}
+# DRAM bytes (read + write) of one launch, from one ncu capture of the bench's
+# workload (profiles/*.md); an entry counts only while the kernel's sources
+# still hash to `src`
+KNOWN_TRAFFIC = {
+    ("topk_softmax", "qwen3_8b_b1"): {"bytes": 4894208, "src": "b7f0f77ebb0463ce"},
+    ("tree_build", "qwen3_8b_b1"): {"bytes": 28928, "src": "90a47972e4415d21"},
+    ("tree_attn", "qwen3_8b_b1"): {"bytes": 17640192, "src": "faa0759cb2c71cf9"},
+    ("accept", "qwen3_8b_b1"): {"bytes": 19471104, "src": "efd9e22f97f71558"}
+}
 KERNEL_SOURCES = {
-    "topk_softmax": ("topk_softmax.cu", "common.cuh"),
+    "topk_softmax": ("topk_softmax.cu", "sm100_ptx.cuh", "common.cuh"),
     "tree_build": ("tree_build.cu", "common.cuh"),
     "tree_attn": ("tree_attn.cu", "sm100_ptx.cuh", "common.cuh"),
-    "accept": ("accept.cu", "common.cuh"),
+    "accept": ("accept.cu", "sm100_ptx.cuh", "common.cuh"),
 }
 
 
@@ -512,7 +517,7 @@ def run_ours(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=40000)   # about 2 s timed: the clock sampler sees the region
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))

@@ -33,9 +33,10 @@
  *   caller zeroes *dev_err and reads it after its own synchronisation.
  * - Calls on different streams are independent as long as they do not share
  *   output buffers or workspaces.
- * - Workspaces (tree_attn, accept) must be zero-filled once when allocated.
- *   Every call leaves them zero-filled again in the words that must start at
- *   zero, so a workspace can be reused without clearing.
+ * - The accept workspace must be zero-filled once when allocated; every call
+ *   leaves it zero-filled again, so it can be reused without clearing.  The
+ *   tree_attn workspace needs no initialisation.  Two calls in flight at the
+ *   same time must not share a workspace.
  */
 #ifndef BASTION_H
 #define BASTION_H
@@ -159,8 +160,12 @@ typedef struct {
   int page_size;              /* paged: tokens per page (16) */
 } bastion_kv_cache;
 
-/* Bytes of workspace bastion_tree_attn needs for these sizes (currently 0:
- * the KV splits merge inside thread-block clusters; the ws argument is kept). */
+/* Bytes of workspace bastion_tree_attn needs for these sizes on the current
+ * device: when the context is split over several CTAs, one partial (O, m, l)
+ * slot of 128 x (d + 4) floats per (request, KV head, 128-row tile, split);
+ * 0 when it is not split.  The value depends on the device (SM count and
+ * cluster occupancy), so query it on the device that runs the call.  Every
+ * call overwrites the slots it reads; the content needs no initialisation. */
 size_t bastion_tree_attn_workspace_size(int B, int n_max, int Hq, int Hkv, int d,
                                         const bastion_kv_cache *kv);
 
@@ -180,7 +185,10 @@ size_t bastion_tree_attn_workspace_size(int B, int n_max, int Hq, int Hkv, int d
  * dtype bf16: tensor-core path (tcgen05, fp32 softmax and accumulation);
  * dtype f32: exact fp32 path.  out has the input dtype; rows i >= n[b] are not
  * written.  Requires d in {64, 128}, Hq % Hkv == 0, n_max <= 256, base
- * pointers 16-byte aligned.  Device errors: BASTION_DEVERR_N, _CTX, _PAGE.
+ * pointers 16-byte aligned.  ws: device workspace of at least
+ * bastion_tree_attn_workspace_size() bytes, 16-byte aligned (may be NULL when
+ * that size is 0), else BASTION_ERR_WORKSPACE.  Device errors:
+ * BASTION_DEVERR_N, _CTX, _PAGE, _TIMEOUT.
  */
 bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *v_tree,
                                  bastion_dtype dtype, int B, int n_max, int Hq, int Hkv, int d,
