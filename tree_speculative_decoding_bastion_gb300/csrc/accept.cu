@@ -101,6 +101,12 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
         bulk_load(k4_smem + off, reinterpret_cast<const uint8_t *>(rowp + c0) + off, nbytes, &s_bar);
       }
     }
+    // while the chunk is in flight: the request's tree, for the walk in case
+    // this CTA completes the request
+    for (int j = tid; j < nb; j += K4_THREADS) {
+      s_par[j] = parent[static_cast<int64_t>(b) * n_max + j];
+      s_tok[j] = token[static_cast<int64_t>(b) * n_max + j];
+    }
     int no_abort = 0;
     if (bytes > 0 && !mbar_wait(&s_bar, 0, &no_abort, K4_WAIT_NS)) {
       if (tid == 0) set_err(dev_err, BASTION_DEVERR_TIMEOUT);
@@ -123,6 +129,10 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
       }
     }
   } else {
+    for (int j = tid; j < nb; j += K4_THREADS) {
+      s_par[j] = parent[static_cast<int64_t>(b) * n_max + j];
+      s_tok[j] = token[static_cast<int64_t>(b) * n_max + j];
+    }
     // unaligned rows: scalar loads, each thread strides over the chunk
     for (int e = c0 + tid; e < c1; e += K4_THREADS) {
       const float x = load_scalar<Tag>(rowp, e);
@@ -139,8 +149,9 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
 #pragma unroll
     for (int w = 1; w < K4_WARPS; ++w) m = s_red[w] > m ? s_red[w] : m;
     if (m) atomicMax(&rowkey[row], m);
-    __threadfence();
-    const uint32_t t = atomicAdd(&tickets[b], 1u);
+    // release: this CTA's row slot update is visible to the CTA that sees the
+    // last ticket; acquire: that CTA then sees every other CTA's update
+    const uint32_t t = atomic_add_acq_rel_gpu(&tickets[b], 1u);
     s_last = (t == static_cast<uint32_t>(nb * C - 1)) ? 1 : 0;
     BST_STAMP(g_k4_trace, 2);
   }
@@ -148,15 +159,12 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
   if (!s_last) return;
 
   // ---- this CTA completed the request: argmax per node, then walk the tree
-  // (the request's argmax, parent and token rows are staged in shared memory
-  // first, so the walk itself touches no global memory)
-  __threadfence();
+  // (argmax, parent and token rows in shared memory: the walk itself touches
+  // no global memory)
   unsigned long long *rk = rowkey + static_cast<int64_t>(b) * n_max;
   for (int j = tid; j < nb; j += K4_THREADS) {
     const int32_t am = packed_i(__ldcg(rk + j));
     s_am[j] = am;
-    s_par[j] = parent[static_cast<int64_t>(b) * n_max + j];
-    s_tok[j] = token[static_cast<int64_t>(b) * n_max + j];
     if (argmax_out) argmax_out[static_cast<int64_t>(b) * n_max + j] = am;
   }
   __syncthreads();

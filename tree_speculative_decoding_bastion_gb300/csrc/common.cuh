@@ -164,6 +164,15 @@ BST_DEV float warp_sum_f(float x) {
   return x;
 }
 
+// Fetch-and-add with acquire-release semantics at GPU scope: the caller's
+// earlier writes (and reductions) are visible to whoever observes the new
+// value, and the caller then sees everything published before the old one.
+BST_DEV uint32_t atomic_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 BST_DEV void set_err(uint32_t *err, uint32_t bit) {
   if (err) atomicOr(err, bit);
 }

@@ -84,6 +84,10 @@ BST_DEV void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+// Split cluster barrier: arrive (no memory ordering) and wait; used to know
+// every CTA of the cluster has started before touching its shared memory.
+BST_DEV void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
+BST_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 BST_DEV void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

@@ -57,14 +57,15 @@ struct K1Smem {
   float new_v[BASTION_MAX_TOPK];
   int32_t new_i[BASTION_MAX_TOPK];
   unsigned long long red[K1_WARPS];
-  float cand_v[K1_CAP + K1_MAXC * BASTION_MAX_TOPK];
-  int32_t cand_i[K1_CAP + K1_MAXC * BASTION_MAX_TOPK];
-  // inbox of CTA rank 0: the partials of every cluster member
+  alignas(16) float cand_v[K1_CAP];
+  alignas(16) int32_t cand_i[K1_CAP];
+  // inbox of CTA rank 0: every cluster member's max, exp-sum and sorted top-k
+  // (entry c * k + j; lists shorter than k are padded with (-inf, INT_MAX))
   float in_m[K1_MAXC];
   float in_s[K1_MAXC];
-  int in_n[K1_MAXC];
-  float in_v[K1_MAXC * BASTION_MAX_TOPK];
-  int32_t in_i[K1_MAXC * BASTION_MAX_TOPK];
+  alignas(16) float in_v[K1_MAXC * BASTION_MAX_TOPK];
+  alignas(16) int32_t in_i[K1_MAXC * BASTION_MAX_TOPK];
+  double L;
 };
 
 // Bitonic sort of one value per lane, descending (lane 0 gets the largest).
@@ -83,19 +84,20 @@ BST_DEV float warp_sort_desc(float v) {
   return v;
 }
 
-// Rank-select: from the M candidates in sm.cand_*, write the best min(k, M) in
-// order into sm.new_* (value desc, index asc).  All threads participate.
-BST_DEV void rank_select(K1Smem &sm, int M, int k) {
-  for (int c = threadIdx.x; c < M; c += K1_THREADS) {
-    const float v = sm.cand_v[c];
-    const int32_t i = sm.cand_i[c];
-    int rank = 0;
-    for (int o = 0; o < M; ++o) rank += better(sm.cand_v[o], sm.cand_i[o], v, i) ? 1 : 0;
-    if (rank < k) {
-      sm.new_v[rank] = v;
-      sm.new_i[rank] = i;
-    }
+// Rank of (v, i) among the M entries (cv, ci): how many are better (value
+// desc, index asc).  Four entries per 16-byte load, all loads independent.
+BST_DEV int rank_among(const float *cv, const int32_t *ci, int M, float v, int32_t i) {
+  int rank = 0;
+  int o = 0;
+#pragma unroll 4
+  for (; o + 4 <= M; o += 4) {
+    const float4 v4 = *reinterpret_cast<const float4 *>(cv + o);
+    const int4 i4 = *reinterpret_cast<const int4 *>(ci + o);
+    rank += static_cast<int>(better(v4.x, i4.x, v, i)) + static_cast<int>(better(v4.y, i4.y, v, i)) +
+            static_cast<int>(better(v4.z, i4.z, v, i)) + static_cast<int>(better(v4.w, i4.w, v, i));
   }
+  for (; o < M; ++o) rank += static_cast<int>(better(cv[o], ci[o], v, i));
+  return rank;
 }
 
 // CTA-wide maximum of a 64-bit key (all threads get it).
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
     }
   }
   __syncthreads();
+  cluster_arrive_relaxed();   // paired with the wait before the first remote store
   pdl_wait();
   pdl_trigger();
   if (tid == 0) BST_STAMP(g_k1_trace, 6);
@@ -226,9 +229,23 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
   __syncthreads();
   if (tid == 0) BST_STAMP(g_k1_trace, 2);
   const int cnt = sm.cnt;
+  cluster_wait();   // every CTA of the cluster has started: rank 0's shared memory exists
+  K1Smem *r0 = cluster.map_shared_rank(&sm, 0);
   if (cnt <= K1_CAP) {
-    rank_select(sm, cnt, k);
-    if (tid == 0) sm.nres = min(k, cnt);
+    // the best k candidates (ranked exactly) go straight to rank 0's inbox
+    for (int c = tid; c < cnt; c += K1_THREADS) {
+      const float v = sm.cand_v[c];
+      const int32_t i = sm.cand_i[c];
+      const int rank = rank_among(sm.cand_v, sm.cand_i, cnt, v, i);
+      if (rank < k) {
+        r0->in_v[crank * k + rank] = v;
+        r0->in_i[crank * k + rank] = i;
+      }
+    }
+    for (int j = cnt + tid; j < k; j += K1_THREADS) {
+      r0->in_v[crank * k + j] = -CUDART_INF_F;
+      r0->in_i[crank * k + j] = 0x7FFFFFFF;
+    }
   } else {
     // Too many ties at the threshold: exact selection by k rounds of
     // "best element strictly after the previous pick".
@@ -253,16 +270,11 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
       }
       ++got;
     }
-    if (tid == 0) sm.nres = got;
-  }
-  __syncthreads();
-
-  // ---- push this CTA's partial into rank 0's inbox, then one cluster barrier
-  K1Smem *r0 = cluster.map_shared_rank(&sm, 0);
-  const int nres = sm.nres;
-  if (tid < nres) {
-    r0->in_v[crank * BASTION_MAX_TOPK + tid] = sm.new_v[tid];
-    r0->in_i[crank * BASTION_MAX_TOPK + tid] = sm.new_i[tid];
+    __syncthreads();
+    if (tid < k) {
+      r0->in_v[crank * k + tid] = tid < got ? sm.new_v[tid] : -CUDART_INF_F;
+      r0->in_i[crank * k + tid] = tid < got ? sm.new_i[tid] : 0x7FFFFFFF;
+    }
   }
   if (tid == 0) {
     float st = 0.f;
@@ -270,59 +282,45 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
     for (int w = 0; w < K1_WARPS; ++w) st += sm.wsum[w];
     r0->in_m[crank] = mt;
     r0->in_s[crank] = st;
-    r0->in_n[crank] = nres;
     BST_STAMP(g_k1_trace, 3);
   }
   cluster.sync();
   if (tid == 0) BST_STAMP(g_k1_trace, 4);
   if (crank != 0) return;
 
-  // ---- rank 0: merge the C partials from its own shared memory
-  __shared__ float s_thr, s_m, s_s;
-  __shared__ int s_cnt;
+  // ---- rank 0: the row's lse, then the top k of the C sorted partial lists
   if (tid < 32) {
     const float mc = (lane < C) ? sm.in_m[lane] : -CUDART_INF_F;
     const float m = warp_max_f(mc);
     const float sc = warp_sum_f((lane < C && mc > -CUDART_INF_F) ? sm.in_s[lane] * expf(mc - m) : 0.f);
-    // every partial list holding k entries bounds the k-th best from below
-    const float th = warp_max_f((lane < C && sm.in_n[lane] == k) ? sm.in_v[lane * BASTION_MAX_TOPK + k - 1]
-                                                                 : -CUDART_INF_F);
     if (lane == 0) {
-      s_m = m;
-      s_s = sc;
-      s_thr = th;
-      s_cnt = 0;
+      // lse = m + ln s with s = 2^e f, f in [0.5, 1): ln s = e ln 2 + ln f keeps
+      // the fp32 logarithm on a small argument (absolute error ~1e-7); only the
+      // final additions run in float64 (this GPU's FP64 pipe is narrow)
+      int e2;
+      const float f = frexpf(sc, &e2);
+      sm.L = static_cast<double>(m) + static_cast<double>(e2) * 0.6931471805599453 + static_cast<double>(logf(f));
     }
   }
   __syncthreads();
-  const float thr2 = s_thr;
-  for (int e = tid; e < C * BASTION_MAX_TOPK; e += K1_THREADS) {
-    const int c = e / BASTION_MAX_TOPK, j = e % BASTION_MAX_TOPK;
-    if (j < sm.in_n[c] && sm.in_v[e] >= thr2) {
-      const int slot = atomicAdd(&s_cnt, 1);
-      sm.cand_v[slot] = sm.in_v[e];
-      sm.cand_i[slot] = sm.in_i[e];
+  const double L = sm.L;
+  const int M = C * k;
+  for (int e = tid; e < M; e += K1_THREADS) {
+    const float v = sm.in_v[e];
+    const int32_t i = sm.in_i[e];
+    if (v == -CUDART_INF_F) continue;
+    const int rank = rank_among(sm.in_v, sm.in_i, M, v, i);
+    if (rank < k) {
+      const int64_t o = static_cast<int64_t>(row) * k + rank;
+      ids[o] = i;
+      lg[o] = v;
+      q[o] = expf(static_cast<float>(static_cast<double>(v) - L));
     }
   }
-  __syncthreads();
-  rank_select(sm, s_cnt, k);
-  __syncthreads();
-  if (tid < k) {
-    // lse = m + ln s with s = 2^e f, f in [0.5, 1): ln s = e ln 2 + ln f keeps
-    // the fp32 logarithm on a small argument (absolute error ~1e-7); only the
-    // final additions run in float64 (this GPU's FP64 pipe is narrow)
-    int e2;
-    const float f = frexpf(s_s, &e2);
-    const double L = static_cast<double>(s_m) + static_cast<double>(e2) * 0.6931471805599453 +
-                     static_cast<double>(logf(f));
-    const int64_t o = static_cast<int64_t>(row) * k + tid;
-    const float v = sm.new_v[tid];
-    ids[o] = sm.new_i[tid];
-    lg[o] = v;
-    q[o] = expf(static_cast<float>(static_cast<double>(v) - L));
-    if (tid == 0) lse[row] = L;
+  if (tid == 0) {
+    lse[row] = L;
+    BST_STAMP(g_k1_trace, 5);
   }
-  if (tid == 0) BST_STAMP(g_k1_trace, 5);
 }
 
 // ---------------------------------------------------------------- launcher
