@@ -62,6 +62,12 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
   if (kBulk && tid == 0) {
     mbar_init(&s_bar, 1);
     fence_mbar_init();
+    // warm L2 with this CTA's chunk of the row while the producing grid finishes
+    const int cb = crank * chunk;
+    const int ln = max(0, min(V, cb + chunk) - cb);
+    if (ln > 0)
+      prefetch_l2_bulk(reinterpret_cast<const T *>(target) + static_cast<int64_t>(row) * row_stride + cb,
+                       static_cast<uint32_t>(ln) * sizeof(T));
   }
   pdl_wait();
   pdl_trigger();

@@ -88,6 +88,13 @@ BST_DEV void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar
 // every CTA of the cluster has started before touching its shared memory.
 BST_DEV void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
 BST_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// L2 prefetch hints (no data returned to the SM, nothing to wait for).  A
+// kernel may issue them before its dependency wait: L2 is the point of
+// coherence, so a later write by the producing grid still wins, and the real
+// loads happen after the wait.
+BST_DEV void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 BST_DEV void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
       fence_mbar_init();
     }
   }
+  // warm L2 with this CTA's chunk while the producing grid finishes
+  if (kBulk && tid == 0 && len > 0) prefetch_l2_bulk(rowp + c0, static_cast<uint32_t>(len) * sizeof(T));
   __syncthreads();
   cluster_arrive_relaxed();   // paired with the wait before the first remote store
   pdl_wait();
