@@ -8,15 +8,19 @@
 // its logits; the accepted path starts at the root and follows the child whose
 // token equals its parent's greedy token.
 //
-// Design (HBM-bound vocabulary pass): the C CTAs of a (request, node) row each
-// stage their contiguous chunk of the row into shared memory with bulk
-// asynchronous copies (cp.async.bulk, all of it in flight at once), then find the
-// chunk's first maximum and publish it as a 64-bit key (value desc, id asc)
-// with one atomicMax on the row's slot in the workspace.  Every CTA then takes a
-// ticket on its request; the CTA that completes the request walks the tree
-// (one warp, ballots over the children), and returns the row slots and the
-// ticket to zero for the next call.  No clusters, no inter-CTA waiting.
+// Design (HBM-bound vocabulary pass): a row is cut into C chunks; CTA
+// (c, b, z) takes chunk c of the rows z, z + Y, ... of request b below its tree
+// size (grid stride, so a small tree in a large budget launches few idle CTAs).
+// Per row it stages the chunk into shared memory with bulk asynchronous copies
+// (cp.async.bulk, all of it in flight at once, the next row prefetched into
+// L2), finds the chunk's first maximum and publishes it as a 64-bit key
+// (value desc, id asc) with one atomicMax on the row's slot in the workspace,
+// then takes a ticket on its request; the CTA that completes the request walks
+// the tree (one warp, ballots over the children), and returns the row slots
+// and the ticket to zero for the next call.  No clusters, no inter-CTA waiting.
 #include <math_constants.h>
+
+#include <algorithm>
 
 #include "sm100_ptx.cuh"
 
@@ -52,22 +56,24 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
   __shared__ int s_last;
   __shared__ int32_t s_am[BASTION_MAX_NODES], s_par[BASTION_MAX_NODES], s_tok[BASTION_MAX_NODES];
 
+  // CTA (crank, b, z) takes chunk crank of the rows z, z + Y, ... of request b
   const int crank = blockIdx.x;
-  const int row = blockIdx.y;
-  const int b = row / n_max;
-  const int i = row - b * n_max;
+  const int b = blockIdx.y;
+  const int z = blockIdx.z;
+  const int Y = gridDim.z;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
+  const T *req = reinterpret_cast<const T *>(target) + static_cast<int64_t>(b) * n_max * row_stride;
+  const int c0 = crank * chunk;
+  const int c1 = min(V, c0 + chunk);
+  const int len = max(0, c1 - c0);
   if (tid == 0) BST_STAMP(g_k4_trace, 0);
   if (kBulk && tid == 0) {
     mbar_init(&s_bar, 1);
     fence_mbar_init();
-    // warm L2 with this CTA's chunk of the row while the producing grid finishes
-    const int cb = crank * chunk;
-    const int ln = max(0, min(V, cb + chunk) - cb);
-    if (ln > 0)
-      prefetch_l2_bulk(reinterpret_cast<const T *>(target) + static_cast<int64_t>(row) * row_stride + cb,
-                       static_cast<uint32_t>(ln) * sizeof(T));
+    // warm L2 with the first chunk while the producing grid finishes
+    if (len > 0 && z < n_max)
+      prefetch_l2_bulk(req + static_cast<int64_t>(z) * row_stride + c0, static_cast<uint32_t>(len) * sizeof(T));
   }
   pdl_wait();
   pdl_trigger();
@@ -75,103 +81,108 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
   const int nb = n_g[b];
 
   if (nb < 1 || nb > n_max) {   // the whole request is invalid
-    if (i == 0 && crank == 0 && tid == 0) {
+    if (z == 0 && crank == 0 && tid == 0) {
       set_err(dev_err, BASTION_DEVERR_N);
       acc_len[b] = -1;
       bonus[b] = -1;
       for (int j = 0; j <= K; ++j) acc_nodes[b * (K + 1) + j] = -1, acc_tok[b * (K + 1) + j] = -1;
     }
-    if (argmax_out && i == 0 && crank == 0)
+    if (argmax_out && z == 0 && crank == 0)
       for (int j = tid; j < n_max; j += K4_THREADS) argmax_out[static_cast<int64_t>(b) * n_max + j] = -1;
     return;
   }
-  if (i >= nb) {
-    if (argmax_out && crank == 0 && tid == 0) argmax_out[row] = -1;
-    return;
-  }
+  if (z >= nb) return;   // no row of this request for this CTA
 
-  const T *rowp = reinterpret_cast<const T *>(target) + static_cast<int64_t>(row) * row_stride;
-  const int c0 = crank * chunk;
-  const int c1 = min(V, c0 + chunk);
-  const int len = max(0, c1 - c0);
-  float bv = -CUDART_INF_F;
-  int32_t bi = -1;
-  if (kBulk) {
-    // ---- stage the chunk into shared memory with bulk copies
-    const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
-    __syncthreads();   // the barrier was initialised before the dependency wait
-    if (tid == 0 && bytes > 0) {
-      mbar_expect_tx(&s_bar, bytes);
-      for (uint32_t off = 0; off < bytes; off += 16384u) {
-        const uint32_t nbytes = min(16384u, bytes - off);
-        bulk_load(k4_smem + off, reinterpret_cast<const uint8_t *>(rowp + c0) + off, nbytes, &s_bar);
-      }
-    }
-    // while the chunk is in flight: the request's tree, for the walk in case
-    // this CTA completes the request
+  if (kBulk) __syncthreads();   // the barrier was initialised before the dependency wait
+
+  // the request's tree, for the walk in case this CTA completes the request
+  auto stage_tree = [&]() {
     for (int j = tid; j < nb; j += K4_THREADS) {
       s_par[j] = parent[static_cast<int64_t>(b) * n_max + j];
       s_tok[j] = token[static_cast<int64_t>(b) * n_max + j];
     }
-    int no_abort = 0;
-    if (bytes > 0 && !mbar_wait(&s_bar, 0, &no_abort, K4_WAIT_NS)) {
-      if (tid == 0) set_err(dev_err, BASTION_DEVERR_TIMEOUT);
-    } else {
-      // thread t scans 16-byte vectors t, t + 256, ... in increasing order, so
-      // a strict ">" keeps its first maximum
-      const uint4 *v4 = reinterpret_cast<const uint4 *>(k4_smem);
-      const int nvec = len / VEC;
-      for (int v = tid; v < nvec; v += K4_THREADS) {
-        const uint4 x = v4[v];
-        const float m = vmax16<Tag>(x);
-        if (m > bv) {
-          int32_t first = -1;
+  };
+  int it = 0;
+  for (int i = z; i < nb; i += Y, ++it) {
+    const int row = b * n_max + i;
+    const T *rowp = req + static_cast<int64_t>(i) * row_stride;
+    float bv = -CUDART_INF_F;
+    int32_t bi = -1;
+    if (kBulk) {
+      // ---- stage the chunk into shared memory with bulk copies
+      const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
+      if (tid == 0 && bytes > 0) {
+        mbar_expect_tx(&s_bar, bytes);
+        for (uint32_t off = 0; off < bytes; off += 16384u) {
+          const uint32_t nbytes = min(16384u, bytes - off);
+          bulk_load(k4_smem + off, reinterpret_cast<const uint8_t *>(rowp + c0) + off, nbytes, &s_bar);
+        }
+        // and warm L2 with this CTA's next row
+        if (i + Y < nb) prefetch_l2_bulk(rowp + static_cast<int64_t>(Y) * row_stride + c0, bytes);
+      }
+      if (it == 0) stage_tree();   // while the first chunk is in flight
+      int no_abort = 0;
+      if (bytes > 0 && !mbar_wait(&s_bar, it & 1, &no_abort, K4_WAIT_NS)) {
+        if (tid == 0) set_err(dev_err, BASTION_DEVERR_TIMEOUT);
+      } else {
+        // thread t scans 16-byte vectors t, t + 256, ... in increasing order, so
+        // a strict ">" keeps its first maximum
+        const uint4 *v4 = reinterpret_cast<const uint4 *>(k4_smem);
+        const int nvec = len / VEC;
+        for (int v = tid; v < nvec; v += K4_THREADS) {
+          const uint4 x = v4[v];
+          const float m = vmax16<Tag>(x);
+          if (m > bv) {
+            int32_t first = -1;
 #pragma unroll
-          for (int j = VEC - 1; j >= 0; --j)
-            if (elem16<Tag>(x, j) == m) first = c0 + v * VEC + j;
-          bv = m;
-          bi = first;
+            for (int j = VEC - 1; j >= 0; --j)
+              if (elem16<Tag>(x, j) == m) first = c0 + v * VEC + j;
+            bv = m;
+            bi = first;
+          }
         }
       }
+    } else {
+      if (it == 0) stage_tree();
+      // unaligned rows: scalar loads, each thread strides over the chunk
+      for (int e = c0 + tid; e < c1; e += K4_THREADS) {
+        const float x = load_scalar<Tag>(rowp, e);
+        if (x > bv) bv = x, bi = e;
+      }
     }
-  } else {
-    for (int j = tid; j < nb; j += K4_THREADS) {
-      s_par[j] = parent[static_cast<int64_t>(b) * n_max + j];
-      s_tok[j] = token[static_cast<int64_t>(b) * n_max + j];
-    }
-    // unaligned rows: scalar loads, each thread strides over the chunk
-    for (int e = c0 + tid; e < c1; e += K4_THREADS) {
-      const float x = load_scalar<Tag>(rowp, e);
-      if (x > bv) bv = x, bi = e;
-    }
-  }
-  if (tid == 0) BST_STAMP(g_k4_trace, 1);
-  unsigned long long key = (bi >= 0) ? pack_vi(bv, bi) : 0ull;
-  key = warp_max_u64(key);
-  if (lane == 0) s_red[tid >> 5] = key;
-  __syncthreads();
-  if (tid == 0) {
-    unsigned long long m = s_red[0];
+    if (tid == 0) BST_STAMP(g_k4_trace, 1);
+    unsigned long long key = (bi >= 0) ? pack_vi(bv, bi) : 0ull;
+    key = warp_max_u64(key);
+    if (lane == 0) s_red[tid >> 5] = key;
+    __syncthreads();   // also: every thread is done with the staged chunk
+    if (tid == 0) {
+      unsigned long long m = s_red[0];
 #pragma unroll
-    for (int w = 1; w < K4_WARPS; ++w) m = s_red[w] > m ? s_red[w] : m;
-    if (m) atomicMax(&rowkey[row], m);
-    // release: this CTA's row slot update is visible to the CTA that sees the
-    // last ticket; acquire: that CTA then sees every other CTA's update
-    const uint32_t t = atomic_add_acq_rel_gpu(&tickets[b], 1u);
-    s_last = (t == static_cast<uint32_t>(nb * C - 1)) ? 1 : 0;
-    BST_STAMP(g_k4_trace, 2);
+      for (int w = 1; w < K4_WARPS; ++w) m = s_red[w] > m ? s_red[w] : m;
+      if (m) atomicMax(&rowkey[row], m);
+      // release: this CTA's row slot update is visible to the CTA that sees the
+      // last ticket; acquire: that CTA then sees every other CTA's update
+      const uint32_t t = atomic_add_acq_rel_gpu(&tickets[b], 1u);
+      s_last = (t == static_cast<uint32_t>(nb * C - 1)) ? 1 : 0;
+      BST_STAMP(g_k4_trace, 2);
+    }
+    __syncthreads();
+    if (s_last) break;   // every (row, chunk) of the request is in: no row remains
   }
-  __syncthreads();
   if (!s_last) return;
 
   // ---- this CTA completed the request: argmax per node, then walk the tree
   // (argmax, parent and token rows in shared memory: the walk itself touches
   // no global memory)
   unsigned long long *rk = rowkey + static_cast<int64_t>(b) * n_max;
-  for (int j = tid; j < nb; j += K4_THREADS) {
-    const int32_t am = packed_i(__ldcg(rk + j));
-    s_am[j] = am;
-    if (argmax_out) argmax_out[static_cast<int64_t>(b) * n_max + j] = am;
+  for (int j = tid; j < n_max; j += K4_THREADS) {
+    if (j < nb) {
+      const int32_t am = packed_i(__ldcg(rk + j));
+      s_am[j] = am;
+      if (argmax_out) argmax_out[static_cast<int64_t>(b) * n_max + j] = am;
+    } else if (argmax_out) {
+      argmax_out[static_cast<int64_t>(b) * n_max + j] = -1;
+    }
   }
   __syncthreads();
   if (tid < 32) {
@@ -223,9 +234,7 @@ cudaError_t launch_accept(const void *target, bool bf16, int B, int n_max, int V
                           const int32_t *n, const int32_t *parent, const int32_t *token, int32_t *acc_len,
                           int32_t *acc_nodes, int32_t *acc_tok, int32_t *bonus, int32_t *argmax_out, void *ws,
                           uint32_t *dev_err, int num_sms, cudaStream_t stream) {
-  (void)num_sms;
   const int esz = bf16 ? 2 : 4;
-  const int rows = B * n_max;
   const int vec = 16 / esz;
   // CTAs per row: chunks of at most 48 KB, each a multiple of 16 bytes
   const int max_chunk = K4_MAX_CHUNK_BYTES / esz;
@@ -237,8 +246,13 @@ cudaError_t launch_accept(const void *target, bool bf16, int B, int n_max, int V
                     ((static_cast<int64_t>(V) * esz) % 16 == 0);
   uint32_t *tickets = reinterpret_cast<uint32_t *>(ws);
   auto *rowkey = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(ws) + accept_ticket_bytes(B));
+  // rows per request handled by Y CTAs each (grid stride): enough CTAs for
+  // about two waves at four per SM, never more than one per row; the tree's
+  // size is a device value, so the grid covers n_max rows
+  const int64_t want = (8LL * num_sms + static_cast<int64_t>(C) * B - 1) / (static_cast<int64_t>(C) * B);
+  const int Y = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(n_max, want)));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, rows, 1);
+  cfg.gridDim = dim3(C, B, Y);
   cfg.blockDim = dim3(K4_THREADS, 1, 1);
   cfg.dynamicSmemBytes = bulk ? static_cast<size_t>(chunk) * esz : 0;
   cfg.stream = stream;

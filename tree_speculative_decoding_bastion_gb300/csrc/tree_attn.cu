@@ -32,7 +32,8 @@
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // BASTION_DEVERR_TIMEOUT, drains what it issued and frees its TMEM.
 //
-// f32 path: an exact fp32 flash-decoding kernel, one CTA per (b, node, head).
+// f32 path: an exact fp32 flash-decoding kernel, one CTA per (b, node, head),
+// 128-key blocks staged in shared memory.
 #include <cooperative_groups.h>
 #include <math_constants.h>
 
@@ -646,10 +647,28 @@ __device__ __forceinline__ const float *f32_ctx_row(const float *base, const Att
   return base + ((static_cast<int64_t>(page) * p.Hkv + kvh) * p.page_size + (j % p.page_size)) * p.d;
 }
 
+// One CTA per (head, node, request): 128-key blocks of the context and then of
+// the tree are staged in shared memory with coalesced loads (K padded by one
+// float per row against bank conflicts), thread t scores key t, and thread e
+// accumulates output element e over the block's keys (online softmax, fp32).
+constexpr int F32_KEYS = 128;
+__host__ __device__ constexpr int f32_smem_bytes(int d) {
+  return (F32_KEYS * (d + 1) + F32_KEYS * d) * 4 + F32_KEYS * 8 * 2 + F32_KEYS * 4;
+}
+
 __global__ void __launch_bounds__(128) tree_attn_f32_kernel(const float *__restrict__ q, const float *__restrict__ kt,
                                                             const float *__restrict__ vt, const float *__restrict__ kc,
                                                             const float *__restrict__ vc, float *__restrict__ out,
                                                             const AttnParamsF32 p) {
+  extern __shared__ __align__(16) float f32s[];
+  const int d = p.d;
+  float *Ks = f32s;                                   // [F32_KEYS][d + 1]
+  float *Vs = Ks + F32_KEYS * (d + 1);                // [F32_KEYS][d]
+  const float **kp = reinterpret_cast<const float **>(Vs + F32_KEYS * d);   // row pointers (NULL: no row)
+  const float **vp = kp + F32_KEYS;
+  float *ps = reinterpret_cast<float *>(vp + F32_KEYS);
+  __shared__ float qs[128];
+  __shared__ float red[4];
   const int h = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   pdl_wait();
@@ -668,34 +687,75 @@ __global__ void __launch_bounds__(128) tree_attn_f32_kernel(const float *__restr
   const int kvh = h / p.g;
   const int W = (p.n_max + 63) >> 6;
   const unsigned long long *mrow = p.mask + (static_cast<int64_t>(b) * p.n_max + i) * W;
-  __shared__ float qs[128];
-  __shared__ float ps[128];
-  __shared__ float red[4];
-  if (tid < p.d) qs[tid] = q[((static_cast<int64_t>(b) * p.n_max + i) * p.Hq + h) * p.d + tid];
-  __syncthreads();
+  if (tid < d) qs[tid] = q[((static_cast<int64_t>(b) * p.n_max + i) * p.Hq + h) * d + tid];
   float m = -CUDART_INF_F, l = 0.f, acc = 0.f;
   const int total = L + nb;
-  for (int base = 0; base < total; base += 128) {
-    const int j = base + tid;
+  for (int base = 0; base < total; base += F32_KEYS) {
+    const int cnt = min(F32_KEYS, total - base);
+    // row pointers of this block's keys; a key is visible when it is a
+    // context key with a valid page or an ancestor (or self) in the tree
+    {
+      const int j = base + tid;
+      const float *kr = nullptr, *vr = nullptr;
+      if (j < L) {
+        bool okp = true;
+        kr = f32_ctx_row(kc, p, b, kvh, j, &okp);
+        vr = f32_ctx_row(vc, p, b, kvh, j, &okp);
+        if (!okp) {
+          set_err(p.dev_err, BASTION_DEVERR_PAGE);
+          kr = vr = nullptr;
+        }
+      } else if (j < total) {
+        const int jt = j - L;
+        if ((mrow[jt >> 6] >> (jt & 63)) & 1ull) {
+          kr = kt + ((static_cast<int64_t>(b) * p.n_max + jt) * p.Hkv + kvh) * d;
+          vr = vt + ((static_cast<int64_t>(b) * p.n_max + jt) * p.Hkv + kvh) * d;
+        }
+      }
+      kp[tid] = kr;
+      vp[tid] = vr;
+    }
+    __syncthreads();
+    // coalesced staging, 16 bytes per load: consecutive threads take
+    // consecutive float4 of a row; eight loads in flight per thread before the
+    // stores (rows are d floats, d a multiple of 4, bases 16-byte aligned)
+    const int d4 = d >> 2;
+    for (int i0 = tid; i0 < cnt * d4; i0 += 128 * 8) {
+      float4 kv[8], vv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = i0 + u * 128;
+        kv[u] = vv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (idx < cnt * d4) {
+          const int row = idx / d4, c = idx - row * d4;
+          const float *kr = kp[row];
+          if (kr) {
+            kv[u] = reinterpret_cast<const float4 *>(kr)[c];
+            vv[u] = reinterpret_cast<const float4 *>(vp[row])[c];
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = i0 + u * 128;
+        if (idx < cnt * d4) {
+          const int row = idx / d4, c = idx - row * d4;
+          float *kd = Ks + row * (d + 1) + 4 * c;
+          kd[0] = kv[u].x;
+          kd[1] = kv[u].y;
+          kd[2] = kv[u].z;
+          kd[3] = kv[u].w;
+          reinterpret_cast<float4 *>(Vs + row * d)[c] = vv[u];
+        }
+      }
+    }
+    __syncthreads();
     float s = -CUDART_INF_F;
-    if (j < L) {
-      bool okp = true;
-      const float *kr = f32_ctx_row(kc, p, b, kvh, j, &okp);
-      if (okp) {
-        float a = 0.f;
-        for (int e = 0; e < p.d; ++e) a = fmaf(qs[e], kr[e], a);
-        s = a * p.scale;
-      } else {
-        set_err(p.dev_err, BASTION_DEVERR_PAGE);
-      }
-    } else if (j < total) {
-      const int jt = j - L;
-      if ((mrow[jt >> 6] >> (jt & 63)) & 1ull) {
-        const float *kr = kt + ((static_cast<int64_t>(b) * p.n_max + jt) * p.Hkv + kvh) * p.d;
-        float a = 0.f;
-        for (int e = 0; e < p.d; ++e) a = fmaf(qs[e], kr[e], a);
-        s = a * p.scale;
-      }
+    if (tid < cnt && kp[tid]) {
+      float a = 0.f;
+      const float *kr = Ks + tid * (d + 1);
+      for (int e = 0; e < d; ++e) a = fmaf(qs[e], kr[e], a);
+      s = a * p.scale;
     }
     float cm = warp_max_f(s);
     if ((tid & 31) == 0) red[tid >> 5] = cm;
@@ -703,37 +763,25 @@ __global__ void __launch_bounds__(128) tree_attn_f32_kernel(const float *__restr
     cm = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     __syncthreads();
     const float m_new = fmaxf(m, cm);
-    if (m_new == -CUDART_INF_F) continue;   // uniform: nothing visible yet
-    const float alpha = expf(m - m_new);
-    const float pj = (s == -CUDART_INF_F) ? 0.f : expf(s - m_new);
-    ps[tid] = pj;
-    float cs = warp_sum_f(pj);
-    if ((tid & 31) == 0) red[tid >> 5] = cs;
-    __syncthreads();
-    cs = red[0] + red[1] + red[2] + red[3];
-    l = l * alpha + cs;
-    acc *= alpha;
-    const int cnt = min(128, total - base);
-    if (tid < p.d) {
-      for (int jj = 0; jj < cnt; ++jj) {
-        const float w = ps[jj];
-        if (w == 0.f) continue;
-        const int jk = base + jj;
-        const float *vr;
-        if (jk < L) {
-          bool okp = true;
-          vr = f32_ctx_row(vc, p, b, kvh, jk, &okp);
-          if (!okp) continue;
-        } else {
-          vr = vt + ((static_cast<int64_t>(b) * p.n_max + (jk - L)) * p.Hkv + kvh) * p.d;
-        }
-        acc = fmaf(w, vr[tid], acc);
+    if (m_new != -CUDART_INF_F) {   // uniform: something is visible
+      const float alpha = expf(m - m_new);
+      const float pj = (s == -CUDART_INF_F) ? 0.f : expf(s - m_new);
+      ps[tid] = pj;
+      float cs = warp_sum_f(pj);
+      if ((tid & 31) == 0) red[tid >> 5] = cs;
+      __syncthreads();
+      cs = red[0] + red[1] + red[2] + red[3];
+      l = l * alpha + cs;
+      acc *= alpha;
+      if (tid < d) {
+#pragma unroll 8
+        for (int jj = 0; jj < cnt; ++jj) acc = fmaf(ps[jj], Vs[jj * d + tid], acc);
       }
+      m = m_new;
     }
-    m = m_new;
     __syncthreads();
   }
-  if (tid < p.d) out[((static_cast<int64_t>(b) * p.n_max + i) * p.Hq + h) * p.d + tid] = acc / l;
+  if (tid < d) out[((static_cast<int64_t>(b) * p.n_max + i) * p.Hq + h) * d + tid] = acc / l;
 }
 
 // ------------------------------------------------------------------ host side
@@ -826,6 +874,8 @@ cudaError_t prepare_tree_attn() {
   if ((e = prefer_max_shared(tree_attn_tc_kernel<128, true>)) != cudaSuccess) return e;
   if ((e = prefer_max_shared(tree_attn_tc_kernel<64, false>)) != cudaSuccess) return e;
   if ((e = prefer_max_shared(tree_attn_tc_kernel<64, true>)) != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tree_attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, f32_smem_bytes(128));
+  if (e != cudaSuccess) return e;
   return prefer_max_shared(tree_attn_f32_kernel);
 }
 
@@ -897,6 +947,7 @@ cudaError_t launch_tree_attn_f32(const float *q, const float *kt, const float *v
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(Hq, n_max, B);
   cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(f32_smem_bytes(d));
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
