@@ -4,12 +4,14 @@ acceptance on one GB300 (or N replicas, one per GPU), printed as one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
-Timed region: K CUDA-graph replays of the four library calls, rotating over
-enough input sets that their total exceeds twice the 129 MB L2 (so every step
-reads its inputs from HBM), bracketed by a barrier and device syncs, timed with
-CUDA events on the launching stream; max over ranks.  Per-kernel durations for
-the roofline come from a second pass of eager launches with events between the
-stages, queued behind a GPU sleep so host launch gaps do not count.
+Timed region: exactly K steps of the four library calls, replayed from CUDA
+graphs (one step per input set in turn), rotating over enough input sets that
+their total exceeds twice the 129 MB L2 (so every step reads its inputs from
+HBM), bracketed by a barrier and device syncs, timed with CUDA events on the
+launching stream; max over ranks.  Per-kernel durations for the roofline come
+from a second pass: each stage launched back to back over the input sets
+between two events, queued behind a GPU sleep so host launch gaps do not count.
+With N > 1 (torchrun) every rank is an independent replica on its own inputs.
 """
 import os
 
@@ -81,6 +83,33 @@ def peaks():
 # ----------------------------------------------------------------------------
 # the oracle on a bounded sample (CPU baseline and the reference arm)
 # ----------------------------------------------------------------------------
+
+
+# ----------------------------------------------------------------------------
+# replicas: one process per GPU, each on its own inputs (weak scaling)
+# ----------------------------------------------------------------------------
+
+
+def replica_seed(rank, r):
+    """Seed of input set r on replica `rank`: every replica draws its own batch."""
+    return 1000 * rank + r
+
+
+def max_over_ranks(x, world):
+    """The largest of the ranks' values (the job's time is its slowest rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, steps, ms):
+    """Whole-job steps/s: every rank ran `steps` steps in at most `ms`."""
+    return world * steps / (ms / 1e3)
 
 
 def oracle_sample_step(inp, target, rows_per_request=64, max_requests=1):
@@ -292,7 +321,7 @@ def run_ours(args, rank, world, local_rank):
     n_sets = args.sets
     r = 0
     while True:
-        inp = I.make_step_inputs(wl, 1000 * rank + r)
+        inp = I.make_step_inputs(wl, replica_seed(rank, r))
         s = dict(inp=inp, logits=up(inp.logits, bf), root=up(inp.root_tok), ctx=up(inp.ctx_len),
                  C=None if inp.C is None else up(inp.C), q=up(inp.q, bf), kt=up(inp.k_tree, bf),
                  vt=up(inp.v_tree, bf))
@@ -369,11 +398,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
     assert int(step.dev_err.item()) == 0, "device error word set during the benchmark"
 
     # ---- per-kernel durations: each stage launched back to back over the
@@ -500,7 +525,7 @@ def run_ours(args, rank, world, local_rank):
                "sample": desc + f"; {len(times)} samples"}
 
     if rank == 0:
-        value = world * args.steps / (ms / 1e3)
+        value = job_throughput(world, args.steps, ms)
         l2 = f"rotating {len(sets)} input sets of {set_bytes / 1e6:.1f} MB (> 2x L2)"
         line = {"metric": "spec-tree steps/s", "value": value, "unit": "steps/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
