@@ -55,7 +55,7 @@ constexpr int ATT_HALF = ATT_N * 128;   // bytes of 128 rows x 64 bf16
 constexpr int ATT_KSTAGES = 3;
 constexpr int ATT_VSTAGES = 3;
 constexpr int ATT_SBUF = 3;             // S / P buffers in TMEM (128 columns each; O follows)
-constexpr int ATT_MAX_SPLITS = 8;       // a portable cluster
+constexpr int ATT_MAX_SPLITS = 16;      // cluster size; above 8 (non-portable) where the device keeps them resident
 constexpr uint64_t ATT_WAIT_NS = 200ull * 1000ull * 1000ull;
 constexpr float ATT_RESCALE_LOG2 = 8.f;
 
@@ -616,7 +616,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
       case 5: merge_splits<D, 5>(p, b, kvh, mtile, split, nb); break;
       case 6: merge_splits<D, 6>(p, b, kvh, mtile, split, nb); break;
       case 7: merge_splits<D, 7>(p, b, kvh, mtile, split, nb); break;
-      default: merge_splits<D, 8>(p, b, kvh, mtile, split, nb); break;
+      case 8: merge_splits<D, 8>(p, b, kvh, mtile, split, nb); break;
+      case 9: merge_splits<D, 9>(p, b, kvh, mtile, split, nb); break;
+      case 10: merge_splits<D, 10>(p, b, kvh, mtile, split, nb); break;
+      case 11: merge_splits<D, 11>(p, b, kvh, mtile, split, nb); break;
+      case 12: merge_splits<D, 12>(p, b, kvh, mtile, split, nb); break;
+      case 13: merge_splits<D, 13>(p, b, kvh, mtile, split, nb); break;
+      case 14: merge_splits<D, 14>(p, b, kvh, mtile, split, nb); break;
+      case 15: merge_splits<D, 15>(p, b, kvh, mtile, split, nb); break;
+      default: merge_splits<D, 16>(p, b, kvh, mtile, split, nb); break;
     }
     if (tid == 0) BST_TRACE_AT(30);
   }
@@ -835,9 +843,10 @@ AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, i
   const int64_t tree_tiles = (n_max + ATT_N - 1) / ATT_N;
   const int64_t units = static_cast<int64_t>(B) * Hkv * pl.mtiles;
   const int64_t tot_tiles = ctx_tiles + tree_tiles;
-  // KV splits per (b, kvh, M-tile), up to a portable cluster of 8: the count
-  // that minimises (waves of resident clusters) x (tiles per CTA + a fixed
-  // cost of about four tiles for set-up, first loads and the merge)
+  // KV splits per (b, kvh, M-tile), up to a cluster of 16 (non-portable sizes
+  // above 8 count only where the device keeps such clusters resident): the
+  // count that minimises (waves of resident clusters) x (tiles per CTA + a
+  // fixed cost of about four tiles for set-up, first loads and the merge)
   int best = 1;
   double best_cost = 1e30;
   for (int s = 1; s <= ATT_MAX_SPLITS; ++s) {
@@ -862,6 +871,13 @@ AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, i
 
 cudaError_t prepare_tree_attn() {
   cudaError_t e;
+  for (const void *fn : {reinterpret_cast<const void *>(tree_attn_tc_kernel<128, false>),
+                         reinterpret_cast<const void *>(tree_attn_tc_kernel<128, true>),
+                         reinterpret_cast<const void *>(tree_attn_tc_kernel<64, false>),
+                         reinterpret_cast<const void *>(tree_attn_tc_kernel<64, true>)}) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   e = cudaFuncSetAttribute(tree_attn_tc_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnLayout<128>::SMEM);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tree_attn_tc_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnLayout<128>::SMEM);
