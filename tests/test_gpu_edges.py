@@ -98,6 +98,27 @@ def test_constant_logits_take_the_tie_path():
     check_tree(tree, o["tree"])
 
 
+@pytest.mark.parametrize("name", ["bf16_v20000", "f32_v1001"])
+def test_topk_streams_more_rows_than_clusters(name):
+    """More drafter rows than clusters fit on the device at once: each cluster
+    streams several rows through its staging buffer and rank 0's two inbox
+    buffers.  Every row is checked against the oracle."""
+    wl = {"bf16_v20000": W["qwen3_8b_b1"].scaled(name="rows_bf16", B=80, K=16, V=20000, topk=8),
+          "f32_v1001": W["tiny_v1024_f32"].scaled(name="rows_f32", B=100, K=8, V=1001, topk=7)}[name]
+    inp = I.make_step_inputs(wl, 3, with_attention=False)
+    R = wl.rows
+    x = I.as_f32(inp.logits, wl.dtype).reshape(R, wl.V)
+    want = dict(zip(("ids", "lg", "q", "lse"), oracle.topk_softmax(x, wl.topk)))
+    got = dict(ids=torch.empty(R, wl.topk, dtype=torch.int32, device="cuda"),
+               lg=torch.empty(R, wl.topk, dtype=torch.float32, device="cuda"),
+               q=torch.empty(R, wl.topk, dtype=torch.float32, device="cuda"),
+               lse=torch.empty(R, dtype=torch.float64, device="cuda"))
+    bn.bastion_topk_softmax(C.dev(inp.logits, wl.dtype).reshape(R, wl.V), wl.topk, got["ids"], got["lg"], got["q"],
+                            got["lse"])
+    torch.cuda.synchronize()
+    check_stage1(wl, {k_: v.cpu().numpy() for k_, v in got.items()}, want)
+
+
 def test_chain_k1():
     """k = 1: the tree is the greedy top-1 chain."""
     wl = W["controller_sweep_peaked"].scaled(name="chain", B=2, V=9000, topk=1, n_min=1, n_max=40, L=100)

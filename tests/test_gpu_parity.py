@@ -224,3 +224,61 @@ def test_attention_and_whole_step_match_oracle(name):
     atol, rtol = attn_tol(wl)
     for r in rows:
         assert np.all(np.abs(got[r] - want[r]) <= atol + rtol * np.abs(want[r])), r
+
+
+def _fill_host(views, inp, target):
+    wl = inp.wl
+    src = {"logits": inp.logits, "root_tok": inp.root_tok, "ctx_len": inp.ctx_len, "q": inp.q, "k_tree": inp.k_tree,
+           "v_tree": inp.v_tree, "target": target}
+    for k_, a in src.items():
+        v = views[k_]
+        if v.dtype == torch.bfloat16:
+            v.view(torch.int16).copy_(torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(v.shape))
+        else:
+            v.copy_(torch.from_numpy(np.ascontiguousarray(a)).view(v.shape))
+
+
+@pytest.mark.parametrize("name", ["qwen3_ragged", "paged_ragged", "qwen3_8b_b1"])
+def test_host_runner_matches_oracle(name):
+    """Steps fed from pinned host blocks through the double-buffered runner:
+    two different drafter/target sets in flight at once (same context cache,
+    latency table and context lengths, which are the runner's fixed state),
+    then a third step that reuses the first slot; every result matches the
+    oracle's."""
+    import dataclasses
+    wl = ALL[name]
+    inp0, o0 = C.pick(wl, 0)
+    sets = [(inp0, o0)]
+    for seed in range(1, 20):   # drafter logits of another seed, without near ties
+        other = I.make_step_inputs(wl, seed, with_attention=False)
+        cand = dataclasses.replace(inp0, logits=other.logits)
+        o = C.oracle_draft(cand)
+        if all(g >= C.GAP for g in o["tree"]["gaps"]):
+            sets.append((cand, o))
+            break
+    assert len(sets) == 2
+    kv = C.kv_of(inp0)
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    step = bn.SpecTreeStep(wl.B, wl.K, wl.V, wl.topk, wl.n_min, wl.n_max, wl.Hq, wl.Hkv, wl.d, kv, act_dtype=dt)
+    Ct = None if inp0.C is None else C.dev(inp0.C)
+    runner = bn.HostStepRunner(step, kv, Ct, inp0.L_AR, inp0.scale, act_dtype=dt, depth=2)
+    wants = []
+    for slot, (inp, o) in enumerate(sets):
+        tree = o["tree"]
+        target = C.target_for(inp, tree)
+        _fill_host(runner.inputs(slot), inp, target)
+        wants.append((tree, C.oracle_accept(inp, tree, target)))
+    order = [0, 1, 0]
+    for s in order[:2]:
+        assert runner.submit() == s
+    got = [runner.collect()]
+    assert runner.submit() == 0
+    got += [runner.collect(), runner.collect()]
+    assert int(step.dev_err.item()) == 0
+    assert runner.h2d_bytes >= sum(v.numel() * v.element_size() for v in runner.inputs(0).values())
+    for s, g in zip(order, got):
+        tree, (acc_len, _, acc_tok, bonus, _) = wants[s]
+        assert np.array_equal(g["n"].numpy(), tree["n"])
+        assert np.array_equal(g["acc_len"].numpy(), acc_len)
+        assert np.array_equal(g["acc_tok"].numpy(), acc_tok)
+        assert np.array_equal(g["bonus"].numpy(), bonus)

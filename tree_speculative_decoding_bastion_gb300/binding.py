@@ -304,7 +304,13 @@ class SpecTreeStep:
         self.q = torch.empty(B, K, topk, **f32)
         self.lse = torch.empty(B, K, dtype=torch.float64, device=dev)
         W = (n_max + 63) // 64
-        self.n = torch.empty(B, **i32)
+        # n, acc_len, bonus and acc_tok share one block, so that a step's
+        # result comes back to the host in a single copy
+        self.result = torch.empty(3 * B + B * (K + 1), **i32)
+        self.n = self.result[0:B]
+        self.acc_len = self.result[B:2 * B]
+        self.bonus = self.result[2 * B:3 * B]
+        self.acc_tok = self.result[3 * B:].view(B, K + 1)
         self.parent = torch.empty(B, n_max, **i32)
         self.token = torch.empty(B, n_max, **i32)
         self.depth = torch.empty(B, n_max, **i32)
@@ -315,10 +321,7 @@ class SpecTreeStep:
         self.S = torch.empty(B, **f32)
         self.S_curve = torch.empty(B, n_max, **f32)
         self.attn_out = torch.empty(B, n_max, Hq, d, dtype=act_dtype, device=dev)
-        self.acc_len = torch.empty(B, **i32)
         self.acc_nodes = torch.empty(B, K + 1, **i32)
-        self.acc_tok = torch.empty(B, K + 1, **i32)
-        self.bonus = torch.empty(B, **i32)
         self.argmax = torch.empty(B, n_max, **i32)
         self.dev_err = torch.zeros(1, **i32)
         self.attn_ws = torch.zeros(max(1, bastion_tree_attn_workspace_size(B, n_max, Hq, Hkv, d, kv)),
@@ -341,3 +344,142 @@ class SpecTreeStep:
     def __call__(self, logits, root_tok, ctx_len, C, L_AR, q, k_tree, v_tree, kv: KV, scale, target, stream=None):
         self.draft(logits, root_tok, ctx_len, C, L_AR, stream=stream)
         self.verify(q, k_tree, v_tree, kv, ctx_len, scale, target, stream=stream)
+
+
+class HostStepRunner:
+    """Spec-tree steps whose per-step inputs come from pinned host memory.
+
+    Each of ``depth`` slots owns a pinned host block and a device block that
+    hold the step's drafter logits, root tokens, context lengths, tree Q/K/V
+    and target logits back to back (each 256-byte aligned), plus a pinned
+    result block.  The caller fills ``inputs(slot)`` (views of the host block)
+    and calls ``submit()``: the host block goes to the device in ``copy_split``
+    equal pieces, each a single copy on its own copy stream (several copy
+    engines in parallel), the step (a CUDA graph of the four library calls, captured
+    once per slot) runs on the compute stream when that copy has landed, and
+    the result block (n, acc_len, bonus, acc_tok) comes back in one copy.  The
+    copy of the next slot overlaps the step in flight.  ``collect()`` waits
+    for the oldest submitted step and returns its result views.
+
+    The context KV cache, the latency table ``C``, ``L_AR`` and the softmax
+    scale are model state: they stay on the device and are fixed per runner.
+    """
+
+    _ALIGN = 256
+
+    def __init__(self, step: SpecTreeStep, kv: KV, C: Optional[torch.Tensor], L_AR: float, scale: float,
+                 act_dtype=torch.bfloat16, depth: int = 2, copy_split: int = 1):
+        if depth < 1:
+            raise BastionError("depth must be >= 1")
+        st = step
+        B, K, V, N, Hq, Hkv, d = st.B, st.K, st.V, st.n_max, st.Hq, st.Hkv, st.d
+        self.step, self.kv, self.C, self.L_AR, self.scale = step, kv, C, float(L_AR), float(scale)
+        self.fields = (("logits", (B, K, V), act_dtype), ("root_tok", (B,), torch.int32),
+                       ("ctx_len", (B,), torch.int32), ("q", (B, N, Hq, d), act_dtype),
+                       ("k_tree", (B, N, Hkv, d), act_dtype), ("v_tree", (B, N, Hkv, d), act_dtype),
+                       ("target", (B, N, V), act_dtype))
+        self.offsets = {}
+        off = 0
+        for name, shape, dt in self.fields:
+            off = (off + self._ALIGN - 1) // self._ALIGN * self._ALIGN
+            self.offsets[name] = off
+            nbytes = torch.Size(shape).numel() * torch.empty(0, dtype=dt).element_size()
+            off += nbytes
+        self.block_bytes = off
+        self.result_numel = st.result.numel()
+        self.depth = depth
+        dev = st.result.device
+        # zero-filled, so that the run made while capturing a slot's graph
+        # reads valid inputs (all-equal logits, empty contexts)
+        self.host = [torch.zeros(off, dtype=torch.uint8, pin_memory=True) for _ in range(depth)]
+        self.dev = [torch.zeros(off, dtype=torch.uint8, device=dev) for _ in range(depth)]
+        self.res_host = [torch.empty(self.result_numel, dtype=torch.int32, pin_memory=True) for _ in range(depth)]
+        self.copy_streams = [torch.cuda.Stream(device=dev) for _ in range(max(1, copy_split))]
+        n = len(self.copy_streams)
+        piece = (off + n - 1) // n
+        piece = (piece + self._ALIGN - 1) // self._ALIGN * self._ALIGN
+        self.pieces = [(a, min(off, a + piece)) for a in range(0, off, piece)]
+        self.stream = torch.cuda.Stream(device=dev)
+        self.copied = [[torch.cuda.Event() for _ in self.pieces] for _ in range(depth)]
+        self.consumed = [torch.cuda.Event() for _ in range(depth)]
+        self.done = [torch.cuda.Event() for _ in range(depth)]
+        self.graphs = [None] * depth
+        self.in_flight = []   # slots submitted and not yet collected, oldest first
+        self.next_slot = 0
+
+    @property
+    def h2d_bytes(self) -> int:
+        return self.block_bytes
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.result_numel * 4
+
+    def _views(self, block: torch.Tensor) -> dict:
+        out = {}
+        for name, shape, dt in self.fields:
+            o = self.offsets[name]
+            nbytes = torch.Size(shape).numel() * torch.empty(0, dtype=dt).element_size()
+            out[name] = block[o:o + nbytes].view(dt).view(shape)
+        return out
+
+    def inputs(self, slot: int) -> dict:
+        """Pinned host views of slot ``slot``'s inputs, to be filled by the caller."""
+        return self._views(self.host[slot])
+
+    def _run(self, slot: int) -> None:
+        v = self._views(self.dev[slot])
+        self.step(v["logits"], v["root_tok"], v["ctx_len"], self.C, self.L_AR, v["q"], v["k_tree"], v["v_tree"],
+                  self.kv, self.scale, v["target"], stream=self.stream)
+
+    def _graph(self, slot: int) -> torch.cuda.CUDAGraph:
+        if self.graphs[slot] is None:
+            torch.cuda.synchronize()
+            with torch.cuda.stream(self.stream):
+                self._run(slot)   # first call outside capture: lazy set-up in the library
+            self.stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                self._run(slot)
+            torch.cuda.synchronize()
+            self.graphs[slot] = g
+        return self.graphs[slot]
+
+    def prepare(self) -> None:
+        """Capture every slot's graph now (otherwise the first submit does)."""
+        for slot in range(self.depth):
+            self._graph(slot)
+
+    def submit(self) -> int:
+        """Start the step of the next slot; returns the slot.  Waits for the
+        oldest step first when all slots are in flight."""
+        if len(self.in_flight) == self.depth:
+            self.collect()
+        slot = self.next_slot
+        self.next_slot = (slot + 1) % self.depth
+        g = self._graph(slot)
+        st = self.stream
+        for (a, b), cs, ev in zip(self.pieces, self.copy_streams, self.copied[slot]):
+            cs.wait_event(self.consumed[slot])   # the step that last read this device block has finished
+            with torch.cuda.stream(cs):
+                self.dev[slot][a:b].copy_(self.host[slot][a:b], non_blocking=True)
+                ev.record(cs)
+        for ev in self.copied[slot]:
+            st.wait_event(ev)
+        with torch.cuda.stream(st):
+            g.replay()
+            self.consumed[slot].record(st)
+            self.res_host[slot].copy_(self.step.result, non_blocking=True)
+            self.done[slot].record(st)
+        self.in_flight.append(slot)
+        return slot
+
+    def collect(self) -> dict:
+        """Wait for the oldest step in flight; its n, acc_len, bonus, acc_tok (host views)."""
+        if not self.in_flight:
+            raise BastionError("no step in flight")
+        slot = self.in_flight.pop(0)
+        self.done[slot].synchronize()
+        r = self.res_host[slot]
+        B, K = self.step.B, self.step.K
+        return {"n": r[0:B], "acc_len": r[B:2 * B], "bonus": r[2 * B:3 * B], "acc_tok": r[3 * B:].view(B, K + 1)}

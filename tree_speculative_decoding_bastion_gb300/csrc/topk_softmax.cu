@@ -139,6 +139,55 @@ BST_DEV void for_each_elem(const uint8_t *stage, const void *rowp, int c0, int l
   }
 }
 
+// Largest element of this thread's share of the staged chunk (16-byte
+// vectors t, t + 512, ...; bf16 pairs compared packed, which is exact).
+template <class Tag>
+BST_DEV float staged_max(const uint8_t *stage, int len) {
+  const uint4 *v4 = reinterpret_cast<const uint4 *>(stage);
+  const int nvec = len / Tag::kVec;
+  float m = -CUDART_INF_F;
+  for (int v = threadIdx.x; v < nvec; v += K1_THREADS) m = fmaxf(m, vmax16<Tag>(v4[v]));
+  return m;
+}
+
+// Pass B over the staged chunk, one 16-byte vector at a time: sum of
+// exp(x - m) for this thread's elements, with x - m (exact for bf16 inputs)
+// and the scale by log2(e) done on float pairs, and the candidates x >= thr
+// appended to the shared list.  The per-element candidate test runs only for
+// a vector whose maximum reaches thr.
+template <class Tag>
+BST_DEV float staged_expsum_candidates(const uint8_t *stage, int c0, int len, float m, float thr, K1Smem &sm) {
+  constexpr int VEC = Tag::kVec;
+  const uint4 *v4 = reinterpret_cast<const uint4 *>(stage);
+  const int nvec = len / VEC;
+  const float2 negm = make_float2(-m, -m);
+  const float2 l2e = make_float2(kLog2e, kLog2e);
+  float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  for (int v = threadIdx.x; v < nvec; v += K1_THREADS) {
+    const uint4 x = v4[v];
+    float f[VEC];
+    unpack16<Tag>(x, f);
+#pragma unroll
+    for (int j = 0; j < VEC; j += 2) {
+      const float2 t = __fmul2_rn(__fadd2_rn(make_float2(f[j], f[j + 1]), negm), l2e);
+      acc[(j >> 1) & 1] = __fadd2_rn(acc[(j >> 1) & 1], make_float2(ex2f(t.x), ex2f(t.y)));
+    }
+    if (vmax16<Tag>(x) >= thr) {
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        if (f[j] >= thr && f[j] > -CUDART_INF_F) {
+          const int slot = atomicAdd(&sm.cnt, 1);
+          if (slot < K1_CAP) {
+            sm.cand_v[slot] = f[j];
+            sm.cand_i[slot] = c0 + v * VEC + j;
+          }
+        }
+      }
+    }
+  }
+  return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+}
+
 template <class Tag, bool kBulk>
 __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
     const void *__restrict__ logits, int V, int64_t row_stride, int k, int chunk,
@@ -192,7 +241,10 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
 
   // ---- pass A: maxima and the candidate threshold
   float tm = -CUDART_INF_F;
-  for_each_elem<Tag, kBulk>(k1_stage, rowp, c0, vlen, [&](float x, int) { tm = fmaxf(tm, x); });
+  if (kBulk)
+    tm = staged_max<Tag>(k1_stage, vlen);
+  else
+    for_each_elem<Tag, kBulk>(k1_stage, rowp, c0, vlen, [&](float x, int) { tm = fmaxf(tm, x); });
   const float sorted = warp_sort_desc(tm);
   const float a_w = __shfl_sync(FULL, sorted, kk - 1);
   const float b_w = __shfl_sync(FULL, sorted, k - 1);
@@ -216,16 +268,20 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
 
   // ---- pass B: exp-sum and candidates
   float s = 0.f;
-  for_each_elem<Tag, kBulk>(k1_stage, rowp, c0, vlen, [&](float x, int idx) {
-    s += ex2f((x - mt) * kLog2e);   // exp(x - m); x - m is exact for bf16 inputs
-    if (x >= thr && x > -CUDART_INF_F) {
-      const int slot = atomicAdd(&sm.cnt, 1);
-      if (slot < K1_CAP) {
-        sm.cand_v[slot] = x;
-        sm.cand_i[slot] = idx;
+  if (kBulk) {
+    s = staged_expsum_candidates<Tag>(k1_stage, c0, vlen, mt, thr, sm);
+  } else {
+    for_each_elem<Tag, kBulk>(k1_stage, rowp, c0, vlen, [&](float x, int idx) {
+      s += ex2f((x - mt) * kLog2e);   // exp(x - m); x - m is exact for bf16 inputs
+      if (x >= thr && x > -CUDART_INF_F) {
+        const int slot = atomicAdd(&sm.cnt, 1);
+        if (slot < K1_CAP) {
+          sm.cand_v[slot] = x;
+          sm.cand_i[slot] = idx;
+        }
       }
-    }
-  });
+    });
+  }
   s = warp_sum_f(s);
   if (lane == 0) sm.wsum[warp] = s;
   __syncthreads();
@@ -329,7 +385,6 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
 cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, int64_t row_stride, int k,
                                 int32_t *ids, float *lg, float *q, double *lse, uint32_t *dev_err, int num_sms,
                                 cudaStream_t stream) {
-  (void)num_sms;
   const int esz = bf16 ? 2 : 4;
   const int vec = 16 / esz;
   // CTAs per row: staged chunks of about 48 KB, at most a portable cluster of 8
@@ -343,10 +398,12 @@ cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, 
   const bool bulk = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((row_stride * esz) % 16 == 0) &&
                     (row_bytes % 16 == 0) && (static_cast<int64_t>(chunk) * esz <= K1_MAX_SMEM);
 
+  (void)num_sms;
+  const size_t dyn = bulk ? static_cast<size_t>(chunk) * esz : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, rows, 1);
   cfg.blockDim = dim3(K1_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = bulk ? static_cast<size_t>(chunk) * esz : 0;
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
@@ -363,14 +420,17 @@ cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, 
 
 cudaError_t prepare_topk_softmax() {
   cudaError_t e;
-  e = cudaFuncSetAttribute(topk_softmax_kernel<BF16Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_MAX_SMEM);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(topk_softmax_kernel<F32Tag, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_MAX_SMEM);
-  if (e != cudaSuccess) return e;
-  if ((e = prefer_max_shared(topk_softmax_kernel<BF16Tag, true>)) != cudaSuccess) return e;
-  if ((e = prefer_max_shared(topk_softmax_kernel<BF16Tag, false>)) != cudaSuccess) return e;
-  if ((e = prefer_max_shared(topk_softmax_kernel<F32Tag, true>)) != cudaSuccess) return e;
-  return prefer_max_shared(topk_softmax_kernel<F32Tag, false>);
+  const void *fns[2][2] = {{reinterpret_cast<const void *>(topk_softmax_kernel<F32Tag, false>),
+                            reinterpret_cast<const void *>(topk_softmax_kernel<F32Tag, true>)},
+                           {reinterpret_cast<const void *>(topk_softmax_kernel<BF16Tag, false>),
+                            reinterpret_cast<const void *>(topk_softmax_kernel<BF16Tag, true>)}};
+  for (int b = 0; b < 2; ++b)
+    for (int u = 0; u < 2; ++u) {
+      e = cudaFuncSetAttribute(fns[b][u], cudaFuncAttributeMaxDynamicSharedMemorySize, K1_MAX_SMEM);
+      if (e != cudaSuccess) return e;
+      if ((e = prefer_max_shared(fns[b][u])) != cudaSuccess) return e;
+    }
+  return cudaSuccess;
 }
 
 }  // namespace bst
