@@ -8,6 +8,7 @@ from .bastion_oracle import (  # noqa: F401
     accept,
     attend,
     context_kv,
+    kv_commit,
     marginals,
     path_to_root,
     stack_trees,

@@ -373,3 +373,50 @@ def accept(target, n, parent, token, K: int):
         acc_tok[b, len(toks)] = int(amax[b, u])
         bonus[b] = int(amax[b, u])
     return acc_len, acc_nodes, acc_tok, bonus, amax
+
+
+# --------------------------------------------------------------------------
+# After acceptance: commit the accepted path's keys and values to the context
+# cache   (FlexDraft page, "Flex-Decoding", decoupled execution: the next draft
+#          reuses the KV cache of the verification pass; [B] "Das Ergebnis":
+#          each step's accepted tokens extend the text)
+# --------------------------------------------------------------------------
+
+
+def kv_commit(k_tree, v_tree, acc_len, acc_nodes, k_ctx, v_ctx, ctx_len, block_table=None, page_size: int = 16):
+    """The context cache after the accepted path of every request joins it.
+
+    For request b with a = acc_len[b] and c = ctx_len[b], the path's nodes
+    acc_nodes[b, 0..a] (root first: the root is the token the previous step
+    emitted, followed by the a accepted draft tokens) are appended at context
+    positions c .. c+a of every KV head, and the context grows to c + a + 1.
+    The root's keys were computed in the verification pass (tree node 0), so
+    it is committed with the accepted drafts; the bonus token becomes the
+    next step's root.
+
+    k_tree/v_tree [B, n_max, Hkv, d]; k_ctx/v_ctx contiguous [B, Hkv, L, d] or
+    paged [P, Hkv, page_size, d] with block_table [B, max_pages] (position p of
+    request b lives in page block_table[b, p // page_size], slot
+    p % page_size).  Returns (k_ctx', v_ctx', ctx_len') as new arrays; the
+    inputs are not modified.
+    """
+    k_new = np.array(k_ctx, copy=True)
+    v_new = np.array(v_ctx, copy=True)
+    B, _, Hkv, _ = np.shape(k_tree)
+    ctx_new = np.array(ctx_len, dtype=np.int32, copy=True)
+    for b in range(B):
+        a = int(acc_len[b])
+        c = int(ctx_len[b])
+        for j in range(a + 1):
+            node = int(acc_nodes[b, j])
+            p = c + j
+            for h in range(Hkv):
+                if block_table is None:
+                    k_new[b, h, p] = k_tree[b, node, h]
+                    v_new[b, h, p] = v_tree[b, node, h]
+                else:
+                    page = int(block_table[b, p // page_size])
+                    k_new[page, h, p % page_size] = k_tree[b, node, h]
+                    v_new[page, h, p % page_size] = v_tree[b, node, h]
+        ctx_new[b] = c + a + 1
+    return k_new, v_new, ctx_new

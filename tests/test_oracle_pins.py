@@ -405,3 +405,91 @@ def test_accept_chain_is_longest_matching_prefix_and_ties_take_lowest_id():
     acc_len, acc_nodes, acc_tok, bonus, amax = oracle.accept(target, np.array([n]), parent, token, 4)
     assert acc_len[0] == 2 and acc_nodes[0].tolist() == [0, 1, 2, -1, -1]
     assert bonus[0] == 0 and acc_tok[0].tolist() == [2, 4, 0, -1, -1]
+
+
+# ---------------------------------------------------------------- KV commit
+
+
+def _with_room(inp, wl, extra):
+    """Context arrays with `extra` more positions of capacity per request
+    (contiguous: longer rows; paged: fresh pages appended to every block-table
+    row)."""
+    f = lambda a: inputs.as_f32(a, wl.dtype).astype(np.float64)
+    kc, vc = f(inp.k_ctx), f(inp.v_ctx)
+    if inp.block_table is None:
+        pad = np.zeros(kc.shape[:2] + (extra,) + kc.shape[3:])
+        return np.concatenate([kc, pad], axis=2), np.concatenate([vc, pad], axis=2), None
+    P = kc.shape[0]
+    per = -(-extra // wl.page_size)
+    new = np.zeros((wl.B * per,) + kc.shape[1:])
+    bt = np.concatenate([inp.block_table, P + np.arange(wl.B * per, dtype=np.int32).reshape(wl.B, per)], axis=1)
+    return np.concatenate([kc, new]), np.concatenate([vc, new]), bt
+
+
+def _first_child_target(T, V):
+    """Target rows whose argmax at every node is the token of its first child,
+    so the accepted path follows first children down to a leaf."""
+    B, N = T["parent"].shape
+    target = np.zeros((B, N, V), np.float32)
+    for b in range(B):
+        n = int(T["n"][b])
+        for u in range(n):
+            kids = [c for c in range(n) if int(T["parent"][b, c]) == u]
+            target[b, u, int(T["token"][b, kids[0]]) if kids else 0] = 1.0
+    return target
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_kv_commit_puts_each_accepted_node_at_its_position(layout):
+    """After the commit, the row at context position pos[i] (stage 2's position
+    of node i) holds node i's key and value for every node i of the accepted
+    path, the context grows by acc_len + 1, and every other cache entry is
+    unchanged."""
+    wl, inp, T, _, f = _small_attention_case(3, layout)
+    kc, vc, bt = _with_room(inp, wl, wl.K + 1)
+    acc_len, acc_nodes, *_ = oracle.accept(_first_child_target(T, wl.V), T["n"], T["parent"], T["token"], wl.K)
+    assert acc_len.max() >= 2   # a path deeper than the root is exercised
+    kt, vt = f(inp.k_tree).astype(np.float64), f(inp.v_tree).astype(np.float64)
+    k2, v2, ctx2 = oracle.kv_commit(kt, vt, acc_len, acc_nodes, kc, vc, inp.ctx_len, block_table=bt,
+                                    page_size=wl.page_size)
+    assert np.array_equal(ctx2, inp.ctx_len + acc_len + 1)
+    touched_k = np.zeros(kc.shape[:-1], bool)
+    for b in range(wl.B):
+        for j in range(int(acc_len[b]) + 1):
+            i = int(acc_nodes[b, j])
+            p = int(T["pos"][b, i])
+            assert T["depth"][b, i] == j and p == inp.ctx_len[b] + j
+            for h in range(wl.Hkv):
+                idx = (b, h, p) if bt is None else (int(bt[b, p // wl.page_size]), h, p % wl.page_size)
+                assert np.array_equal(k2[idx], kt[b, i, h]) and np.array_equal(v2[idx], vt[b, i, h])
+                touched_k[idx] = True
+    assert np.array_equal(k2[~touched_k], kc[~touched_k]) and np.array_equal(v2[~touched_k], vc[~touched_k])
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_kv_commit_context_attention_equals_tree_attention(layout):
+    """For every accepted node at depth j, plain attention of its query over the
+    first ctx_len + j + 1 positions of the committed cache (keys gathered here
+    by explicit page lookups, softmax by torch) equals the tree attention the
+    verification pass computed for it: the committed prefix is exactly the key
+    set that node saw."""
+    wl, inp, T, out, f = _small_attention_case(5, layout)
+    kc, vc, bt = _with_room(inp, wl, wl.K + 1)
+    acc_len, acc_nodes, *_ = oracle.accept(_first_child_target(T, wl.V), T["n"], T["parent"], T["token"], wl.K)
+    kt, vt, q = (f(a).astype(np.float64) for a in (inp.k_tree, inp.v_tree, inp.q))
+    k2, v2, _ = oracle.kv_commit(kt, vt, acc_len, acc_nodes, kc, vc, inp.ctx_len, block_table=bt,
+                                 page_size=wl.page_size)
+    g = wl.Hq // wl.Hkv
+    for b in range(wl.B):
+        for j in range(int(acc_len[b]) + 1):
+            i = int(acc_nodes[b, j])
+            L = int(inp.ctx_len[b]) + j + 1
+            for h in range(wl.Hq):
+                kvh = h // g
+                if bt is None:
+                    ck, cv = k2[b, kvh, :L], v2[b, kvh, :L]
+                else:
+                    ck = np.stack([k2[bt[b, t // wl.page_size], kvh, t % wl.page_size] for t in range(L)])
+                    cv = np.stack([v2[bt[b, t // wl.page_size], kvh, t % wl.page_size] for t in range(L)])
+                np.testing.assert_allclose(_sdpa(q[b, i, h], ck, cv, inp.scale), out[b, i, h], rtol=1e-10,
+                                           atol=1e-12)
