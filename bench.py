@@ -480,6 +480,59 @@ def run_ours(args, rank, world, local_rank):
             e["tensor_frac"] = e["TFLOP/s"] / tf_burst
         stages[k] = e
 
+    # ---- beyond the step: commit the accepted path of set 0 to a scratch
+    # cache laid out like the workload's (contiguous rows with room, or fresh
+    # pages for the positions the commit writes), so the workload's own
+    # context stays fixed; timed alone, back to back
+    commit = None
+    if not args.no_commit:
+        s = sets[0]
+        with torch.cuda.stream(stream):
+            step(*args_of(s))
+        torch.cuda.synchronize()
+        ctx_h = s["ctx"].cpu().numpy()
+        acc_h = step.acc_len.cpu().numpy()
+        esz = 2 if bf else 4
+        if s["inp"].block_table is None:
+            shape = (wl.B, wl.Hkv, int(ctx_h.max()) + wl.K + 1, wl.d)
+            kv_s = bn.KV(torch.zeros(shape, dtype=dt, device="cuda"), torch.zeros(shape, dtype=dt, device="cuda"))
+        else:
+            ps = wl.page_size
+            cols = (int(ctx_h.max()) + wl.K + ps) // ps
+            bt = np.zeros((wl.B, cols), np.int32)
+            npg = 0
+            for b in range(wl.B):
+                for col in range(int(ctx_h[b]) // ps, (int(ctx_h[b]) + wl.K) // ps + 1):
+                    bt[b, col] = npg
+                    npg += 1
+            shape = (npg, wl.Hkv, ps, wl.d)
+            kv_s = bn.KV(torch.zeros(shape, dtype=dt, device="cuda"), torch.zeros(shape, dtype=dt, device="cuda"),
+                         up(bt))
+        ctx_out = torch.empty_like(s["ctx"])
+
+        def commit_once():
+            bn.bastion_kv_commit(s["kt"], s["vt"], kv_s, step.acc_len, step.acc_nodes, s["ctx"], ctx_out,
+                                 dev_err=step.dev_err, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                commit_once()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            torch.cuda._sleep(int(10e6))
+            ev[0].record(stream)
+            for _ in range(200):
+                commit_once()
+            ev[1].record(stream)
+        torch.cuda.synchronize()
+        assert int(step.dev_err.item()) == 0, "device error word set by the commit"
+        assert np.array_equal(ctx_out.cpu().numpy(), ctx_h + acc_h + 1)
+        c_us = ev[0].elapsed_time(ev[1]) * 1e3 / 200
+        rows = int((acc_h + 1).sum()) * wl.Hkv * 2
+        cbytes = rows * wl.d * esz * 2
+        commit = {"avg_us": c_us, "rows": rows, "bytes_per_launch": cbytes, "GB/s": cbytes / (c_us * 1e-6) / 1e9,
+                  "note": "bastion_kv_commit of set 0's accepted paths (acc_len + 1 rows per request and KV head, "
+                          "K and V), bytes read + written; not part of the step"}
+
     # ---- end to end through the public API from pinned host buffers: every
     # step copies its whole input block host -> device and its result block
     # back; the runner keeps two slots so one step's copy overlaps the other's
@@ -533,7 +586,8 @@ def run_ours(args, rank, world, local_rank):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf else "f32",
                 "data": "synthetic", "config": config_of(wl, l2), "roofline": roof, "stages": stages,
-                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+                "cpu_baseline": cpu, "e2e": e2e, "next_rows": {"kv_commit": commit},
+                "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk, "tree": {"n": [int(x) for x in nb],
                                         "ahat": [float(x) for x in step.ahat.cpu().numpy()],
                                         "acc_len": [int(x) for x in step.acc_len.cpu().numpy()]},
@@ -550,6 +604,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = enough for 2x L2)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-commit", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()

@@ -253,6 +253,37 @@ bastion_status bastion_accept_noalloc(const void *target, bastion_dtype dtype, i
                                       int32_t *acc_tok, int32_t *bonus, int32_t *argmax_out,
                                       uint32_t *dev_err, bastion_stream_t stream);
 
+/*
+ * After acceptance -- commit the accepted path's keys and values to the
+ * context cache (FlexDraft page, "Flex-Decoding", decoupled execution: drafting
+ * continues from the verified prefix and reuses the verification pass's KV
+ * cache; BASTION page, "Das Ergebnis": each step's accepted tokens extend the
+ * text).
+ *
+ * For request b with a = acc_len[b] and c = ctx_len[b]: for j = 0..a and every
+ * KV head h, the rows k_tree[b, acc_nodes[b, j], h, :] and v_tree[...] are
+ * written at context position c + j of kv (contiguous: [b, h, c + j, :];
+ * paged: page block_table[b, (c + j) / page_size], slot (c + j) % page_size),
+ * and ctx_out[b] = c + a + 1.  acc_nodes is bastion_accept's path, root first:
+ * the root (the token the previous step emitted, keyed by this step's
+ * verification pass at position c) and the a accepted draft tokens; the bonus
+ * token is the next step's root.  Other cache entries are not touched.
+ * Layouts: k_tree, v_tree [B, n_max, Hkv, d] (dtype elements); acc_len, ctx_len,
+ * ctx_out int32 [B]; acc_nodes int32 [B, K+1]; kv as for bastion_tree_attn,
+ * whose k and v buffers this call WRITES (the struct's const qualifies the
+ * attention call).  ctx_out may alias ctx_len (in-place advance).
+ * Requires d * sizeof(dtype) a multiple of 16 bytes, d <= 512, n_max <= 256,
+ * K <= 32, B <= 65535, 16-byte aligned k_tree, v_tree, kv->k, kv->v.
+ * Device errors (the request copies nothing and ctx_out[b] = ctx_len[b]):
+ * acc_len[b] outside [0, K] or a path node outside [0, n_max)
+ * (BASTION_DEVERR_N); ctx_len[b] < 0 or c + a beyond the cache capacity
+ * (BASTION_DEVERR_CTX); a page id outside [0, num_pages) (BASTION_DEVERR_PAGE).
+ */
+bastion_status bastion_kv_commit(const void *k_tree, const void *v_tree, bastion_dtype dtype, int B, int n_max,
+                                 int Hkv, int d, int K, const int32_t *acc_len, const int32_t *acc_nodes,
+                                 const bastion_kv_cache *kv, const int32_t *ctx_len, int32_t *ctx_out,
+                                 uint32_t *dev_err, bastion_stream_t stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

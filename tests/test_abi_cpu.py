@@ -129,3 +129,31 @@ def test_workspace_sizes_are_zero_without_a_device(L):
         pytest.skip("a GPU is present; sizes are device-dependent")
     assert L.bastion_accept_workspace_size(2, 64) >= 2 * 64 * 4
     assert L.bastion_init(0) == NO_DEVICE
+
+
+def test_kv_commit_rejects_bad_arguments(L):
+    from tree_speculative_decoding_bastion_gb300.binding import KVCache
+    f = L.bastion_kv_commit
+    kv = KVCache()
+    kv.k, kv.v, kv.L_max = 16, 16, 4096
+
+    def call(**kw):
+        a = dict(kt=P, dt=1, B=2, N=64, H=8, d=128, K=16, ctx_out=P)
+        a.update(kw)
+        return f(a["kt"], P, a["dt"], a["B"], a["N"], a["H"], a["d"], a["K"], P, P, ctypes.byref(kv), P,
+                 a["ctx_out"], None, None)
+
+    assert call(kt=None) == INVALID
+    assert call(ctx_out=None) == INVALID
+    assert call(dt=5) == INVALID
+    assert call(B=0) == INVALID
+    assert call(N=300) == UNSUPPORTED
+    assert call(K=33) == UNSUPPORTED
+    assert call(d=4) == UNSUPPORTED            # 8 bytes per bf16 row: not a multiple of 16
+    assert call(kt=ctypes.c_void_p(24)) == INVALID   # not 16-byte aligned
+    kv.L_max = 0
+    assert call() == INVALID
+    kv.L_max = 4096
+    kv.block_table = 16
+    kv.max_pages, kv.num_pages, kv.page_size = 0, 8, 16
+    assert call() == INVALID

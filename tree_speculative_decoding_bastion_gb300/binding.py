@@ -56,6 +56,8 @@ _SIGS = {
                                 _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p, _c_p]),
     "bastion_accept_noalloc": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_p, _c_p, _c_p,
                                         _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "bastion_kv_commit": (_c_int, [_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p,
+                                   ctypes.POINTER(KVCache), _c_p, _c_p, _c_p, _c_p]),
 }
 
 _lib = None
@@ -281,6 +283,37 @@ def bastion_accept_noalloc(target, n, parent, token, K: int, acc_len, acc_nodes,
                                         _ptr(n), _ptr(parent), _ptr(token), _ptr(acc_len), _ptr(acc_nodes),
                                         _ptr(acc_tok), _ptr(bonus), _ptr(argmax_out), _ptr(dev_err),
                                         _stream(stream)), "bastion_accept_noalloc")
+
+
+def bastion_kv_commit(k_tree, v_tree, kv: "KV", acc_len, acc_nodes, ctx_len, ctx_out, dev_err=None,
+                      stream=None) -> None:
+    """After acceptance: append each request's accepted path (acc_nodes, root
+    first, acc_len + 1 nodes) to the context cache at positions ctx_len ..
+    ctx_len + acc_len and set ctx_out = ctx_len + acc_len + 1 (ctx_out may be
+    ctx_len).  k_tree/v_tree [B, n_max, Hkv, d] (the cache's dtype);
+    acc_nodes int32 [B, K+1]; acc_len, ctx_len, ctx_out int32 [B].  kv's k and v
+    are written."""
+    B, N, Hkv, d = k_tree.shape
+    dt = k_tree.dtype
+    _need(k_tree, dt, None, "k_tree")
+    _need(v_tree, dt, (B, N, Hkv, d), "v_tree")
+    _need(kv.k, dt, None, "kv.k")
+    _need(kv.v, dt, tuple(kv.k.shape), "kv.v")
+    if kv.block_table is not None:
+        _need(kv.block_table, torch.int32, None, "block_table")
+    _need(acc_len, torch.int32, (B,), "acc_len")
+    if acc_nodes.dim() != 2 or acc_nodes.shape[0] != B:
+        raise BastionError("acc_nodes must be [B, K+1]")
+    _need(acc_nodes, torch.int32, None, "acc_nodes")
+    K = acc_nodes.shape[1] - 1
+    _need(ctx_len, torch.int32, (B,), "ctx_len")
+    _need(ctx_out, torch.int32, (B,), "ctx_out")
+    if dev_err is not None:
+        _need(dev_err, torch.int32, (1,), "dev_err")
+    s = kv.c_struct()
+    _check(lib().bastion_kv_commit(_ptr(k_tree), _ptr(v_tree), _dtype_code(k_tree), B, N, Hkv, d, K, _ptr(acc_len),
+                                   _ptr(acc_nodes), ctypes.byref(s), _ptr(ctx_len), _ptr(ctx_out), _ptr(dev_err),
+                                   _stream(stream)), "bastion_kv_commit")
 
 
 # --------------------------------------------------------------------------

@@ -47,6 +47,10 @@ cudaError_t launch_tree_attn_f32(const float *q, const float *kt, const float *v
                                  int64_t L_max, int page_size, int max_pages, int num_pages, int64_t cap,
                                  const int32_t *ctx_len, const int32_t *n, const uint64_t *mask,
                                  const int32_t *block_table, uint32_t *dev_err, cudaStream_t stream);
+cudaError_t launch_kv_commit(const void *k_tree, const void *v_tree, int esz, int B, int n_max, int Hkv, int d, int K,
+                             const int32_t *acc_len, const int32_t *acc_nodes, void *kc, void *vc, int64_t L_max,
+                             const int32_t *block_table, int max_pages, int num_pages, int page_size,
+                             const int32_t *ctx_len, int32_t *ctx_out, uint32_t *dev_err, cudaStream_t stream);
 }  // namespace bst
 
 namespace {
@@ -337,6 +341,39 @@ bastion_status bastion_accept(const void *target, bastion_dtype dtype, int B, in
                                      acc_len, acc_nodes, acc_tok, bonus, argmax_out, ws, dev_err, sms,
                                      reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "accept launch");
+  return BASTION_OK;
+}
+
+bastion_status bastion_kv_commit(const void *k_tree, const void *v_tree, bastion_dtype dtype, int B, int n_max, int Hkv,
+                                 int d, int K, const int32_t *acc_len, const int32_t *acc_nodes,
+                                 const bastion_kv_cache *kv, const int32_t *ctx_len, int32_t *ctx_out,
+                                 uint32_t *dev_err, bastion_stream_t stream) {
+  if (!k_tree || !v_tree || !acc_len || !acc_nodes || !kv || !kv->k || !kv->v || !ctx_len || !ctx_out)
+    return fail(BASTION_ERR_INVALID_ARG, "kv_commit: NULL pointer");
+  if (dtype != BASTION_F32 && dtype != BASTION_BF16) return fail(BASTION_ERR_INVALID_ARG, "kv_commit: bad dtype");
+  if (B < 1 || n_max < 1 || Hkv < 1 || d < 1 || K < 1) return fail(BASTION_ERR_INVALID_ARG, "kv_commit: bad sizes");
+  if (n_max > BASTION_MAX_NODES || K > BASTION_MAX_DEPTH || d > 512 || B > 65535)
+    return fail(BASTION_ERR_UNSUPPORTED, "kv_commit: n_max <= 256, K <= 32, d <= 512, B <= 65535");
+  const int esz = dtype == BASTION_BF16 ? 2 : 4;
+  if ((d * esz) % 16 != 0) return fail(BASTION_ERR_UNSUPPORTED, "kv_commit: a row of d elements must be a multiple of 16 bytes");
+  if (!aligned16(k_tree) || !aligned16(v_tree) || !aligned16(kv->k) || !aligned16(kv->v))
+    return fail(BASTION_ERR_INVALID_ARG, "kv_commit: tensors must be 16-byte aligned");
+  const bool paged = kv->block_table != nullptr;
+  if (paged) {
+    if (kv->max_pages < 1 || kv->num_pages < 1 || kv->page_size < 1)
+      return fail(BASTION_ERR_INVALID_ARG, "kv_commit: bad page counts");
+  } else if (kv->L_max < 1) {
+    return fail(BASTION_ERR_INVALID_ARG, "kv_commit: L_max must be >= 1");
+  }
+  int sms = 0;
+  bastion_status s = current_device(&sms);
+  if (s != BASTION_OK) return s;
+  // the cache is written: the struct's const qualifies the attention call's view
+  cudaError_t e = bst::launch_kv_commit(k_tree, v_tree, esz, B, n_max, Hkv, d, K, acc_len, acc_nodes,
+                                        const_cast<void *>(kv->k), const_cast<void *>(kv->v), kv->L_max,
+                                        kv->block_table, kv->max_pages, kv->num_pages, kv->page_size, ctx_len,
+                                        ctx_out, dev_err, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_commit launch");
   return BASTION_OK;
 }
 
