@@ -7,9 +7,11 @@ from .bastion_oracle import (  # noqa: F401
     Tree,
     accept,
     attend,
+    block_mask,
     context_kv,
     kv_commit,
     marginals,
+    masked_attention,
     path_to_root,
     stack_trees,
     topk_softmax,

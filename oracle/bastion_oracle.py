@@ -420,3 +420,52 @@ def kv_commit(k_tree, v_tree, acc_len, acc_nodes, k_ctx, v_ctx, ctx_len, block_t
                     v_new[page, h, p % page_size] = v_tree[b, node, h]
         ctx_new[b] = c + a + 1
     return k_new, v_new, ctx_new
+
+
+# --------------------------------------------------------------------------
+# Block-diffusion drafter mask   (FlexDraft page, "Attention-Tuning": mask
+#          tokens appended to the clean prefix attend bidirectionally inside
+#          their block and to the clean prefix, and stay isolated from other
+#          blocks; BASTION Methodik §1: the drafter fills a block of positions
+#          in one pass)
+# --------------------------------------------------------------------------
+
+
+def block_mask(n, n_max: int, block: int) -> np.ndarray:
+    """uint64 [B, n_max, ceil(n_max/64)]: for request b and row i < n[b], bit j
+    is set iff j < n[b] and j and i lie in the same block of `block`
+    consecutive positions (i // block == j // block); rows i >= n[b] are 0."""
+    B = len(n)
+    W = (n_max + 63) // 64
+    mask = np.zeros((B, n_max, W), dtype=np.uint64)
+    for b in range(B):
+        nb = int(n[b])
+        for i in range(nb):
+            for j in range(nb):
+                if i // block == j // block:
+                    mask[b, i, j // 64] |= np.uint64(1) << np.uint64(j % 64)
+    return mask
+
+
+def masked_attention(q, k_tree, v_tree, k_ctx, v_ctx, ctx_len, mask, n, Hkv: int, scale: float,
+                     block_table=None, page_size: int = 16, rows=None) -> np.ndarray:
+    """Attention of rows i < n[b] over the context and the positions j whose
+    bit is set in mask[b, i] (ascending j), float64; NaN for rows not computed.
+    Shapes as in tree_attention; ``rows`` optionally lists the (b, i, h) to do."""
+    B, N, Hq, d = q.shape
+    g = Hq // Hkv
+    out = np.full((B, N, Hq, d), np.nan, dtype=np.float64)
+    if rows is None:
+        rows = [(b, i, h) for b in range(B) for i in range(int(n[b])) for h in range(Hq)]
+    cache = {}
+    for (b, i, h) in sorted(rows, key=lambda r: (r[0], r[2] // g, r[1], r[2])):
+        kvh = h // g
+        if (b, kvh) not in cache:
+            cache.clear()
+            cache[(b, kvh)] = context_kv(k_ctx, v_ctx, block_table, b, kvh, int(ctx_len[b]), page_size)
+        kc, vc = cache[(b, kvh)]
+        sel = [j for j in range(N) if (int(mask[b, i, j // 64]) >> (j % 64)) & 1]
+        keys = np.concatenate([kc, np.asarray(k_tree[b, sel, kvh], dtype=np.float64)])
+        values = np.concatenate([vc, np.asarray(v_tree[b, sel, kvh], dtype=np.float64)])
+        out[b, i, h] = attend(q[b, i, h], keys, values, scale)
+    return out

@@ -493,3 +493,53 @@ def test_kv_commit_context_attention_equals_tree_attention(layout):
                     cv = np.stack([v2[bt[b, t // wl.page_size], kvh, t % wl.page_size] for t in range(L)])
                 np.testing.assert_allclose(_sdpa(q[b, i, h], ck, cv, inp.scale), out[b, i, h], rtol=1e-10,
                                            atol=1e-12)
+
+
+# ---------------------------------------------------------------- drafter mask
+
+
+def test_block_mask_bits_by_definition():
+    """Bits written out from the definition (same block, inside n) for ragged
+    n, a block that does not divide n, and rows past n."""
+    n = np.array([1, 37, 70])
+    m = oracle.block_mask(n, 80, 16)
+    assert m.shape == (3, 80, 2) and m.dtype == np.uint64
+    for b, nb in enumerate(n):
+        for i in range(80):
+            bits = {j for j in range(80) if (int(m[b, i, j // 64]) >> (j % 64)) & 1}
+            want = {j for j in range(nb) if j // 16 == i // 16} if i < nb else set()
+            assert bits == want, (b, i)
+
+
+def test_masked_attention_with_ancestor_mask_is_tree_attention():
+    """With stage 2's ancestor-or-self mask, masked attention reproduces the
+    tree attention of the same tree (which walks parents instead)."""
+    for layout in ("contiguous", "paged"):
+        wl, inp, T, out, f = _small_attention_case(2, layout)
+        got = oracle.masked_attention(f(inp.q), f(inp.k_tree), f(inp.v_tree), f(inp.k_ctx), f(inp.v_ctx),
+                                      inp.ctx_len, T["mask"], T["n"], wl.Hkv, inp.scale,
+                                      block_table=inp.block_table, page_size=wl.page_size)
+        np.testing.assert_allclose(got, out, rtol=1e-12, atol=1e-13, equal_nan=True)
+
+
+def test_one_block_is_unmasked_attention_and_unit_blocks_see_themselves():
+    """A block spanning all n rows: every row attends to the whole context and
+    every block position (torch SDPA without a mask); blocks of one with no
+    context: each row's output is its own value row."""
+    rng = np.random.default_rng(8)
+    B, N, Hq, Hkv, d, L = 1, 12, 4, 2, 8, 9
+    q = rng.standard_normal((B, N, Hq, d))
+    kt, vt = rng.standard_normal((B, N, Hkv, d)), rng.standard_normal((B, N, Hkv, d))
+    kc, vc = rng.standard_normal((B, Hkv, L, d)), rng.standard_normal((B, Hkv, L, d))
+    n = np.array([10])
+    out = oracle.masked_attention(q, kt, vt, kc, vc, np.array([L]), oracle.block_mask(n, N, 16), n, Hkv, 0.4)
+    for i in range(10):
+        for h in range(Hq):
+            keys = np.concatenate([kc[0, h // 2], kt[0, :10, h // 2]])
+            vals = np.concatenate([vc[0, h // 2], vt[0, :10, h // 2]])
+            np.testing.assert_allclose(out[0, i, h], _sdpa(q[0, i, h], keys, vals, 0.4), rtol=1e-12, atol=1e-13)
+    solo = oracle.masked_attention(q, kt, vt, kc, vc, np.array([0]), oracle.block_mask(n, N, 1), n, Hkv, 0.4)
+    for i in range(10):
+        for h in range(Hq):
+            np.testing.assert_allclose(solo[0, i, h], vt[0, i, h // 2], rtol=1e-14)
+    assert np.all(np.isnan(solo[0, 10:]))
