@@ -533,6 +533,40 @@ def run_ours(args, rank, world, local_rank):
                   "note": "bastion_kv_commit of set 0's accepted paths (acc_len + 1 rows per request and KV head, "
                           "K and V), bytes read + written; not part of the step"}
 
+    # ---- beyond the step: the drafter's attention over the same context, one
+    # block of K mask tokens per request (block-diffusion mask built on the
+    # device, then the attention call driven by it); timed alone
+    drafter = None
+    if not args.no_commit:
+        s = sets[0]
+        n_blk = torch.full((wl.B,), wl.K, dtype=torch.int32, device="cuda")
+        dmask = torch.empty_like(step.mask)
+        dout = torch.empty_like(step.attn_out)
+
+        def drafter_once():
+            bn.bastion_block_mask(n_blk, wl.K, dmask, dev_err=step.dev_err, stream=stream)
+            bn.bastion_tree_attn(s["q"], s["kt"], s["vt"], s["kv"], s["ctx"], dmask, n_blk, dout, s["inp"].scale,
+                                 ws=step.attn_ws, dev_err=step.dev_err, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                drafter_once()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            torch.cuda._sleep(int(10e6))
+            ev[0].record(stream)
+            for _ in range(100):
+                drafter_once()
+            ev[1].record(stream)
+        torch.cuda.synchronize()
+        assert int(step.dev_err.item()) == 0, "device error word set by the drafter attention"
+        d_us = ev[0].elapsed_time(ev[1]) * 1e3 / 100
+        esz = 2 if bf else 4
+        ctx_bytes = int(sum(int(x) for x in s["inp"].ctx_len)) * wl.Hkv * wl.d * esz * 2
+        drafter = {"avg_us": d_us, "rows": wl.B * wl.K * wl.Hq, "context_bytes": ctx_bytes,
+                   "GB/s": ctx_bytes / (d_us * 1e-6) / 1e9,
+                   "note": "bastion_block_mask + bastion_tree_attn: B requests x one block of K mask tokens over "
+                           "the workload's context (bidirectional inside the block); not part of the step"}
+
     # ---- end to end through the public API from pinned host buffers: every
     # step copies its whole input block host -> device and its result block
     # back; the runner keeps two slots so one step's copy overlaps the other's
@@ -586,7 +620,7 @@ def run_ours(args, rank, world, local_rank):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf else "f32",
                 "data": "synthetic", "config": config_of(wl, l2), "roofline": roof, "stages": stages,
-                "cpu_baseline": cpu, "e2e": e2e, "next_rows": {"kv_commit": commit},
+                "cpu_baseline": cpu, "e2e": e2e, "next_rows": {"kv_commit": commit, "drafter_attention": drafter},
                 "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk, "tree": {"n": [int(x) for x in nb],
                                         "ahat": [float(x) for x in step.ahat.cpu().numpy()],

@@ -13,6 +13,11 @@
  *                                                                        "baumgestützte Verifizierung")
  *   bastion_accept        greedy (temperature 0) acceptance             (Experimentelle Ergebnisse)
  *
+ * and, around the step:
+ *
+ *   bastion_kv_commit     the accepted path joins the context KV cache  (FlexDraft page, "Flex-Decoding")
+ *   bastion_block_mask    block-diffusion drafter mask for the attention (FlexDraft page, "Attention-Tuning")
+ *
  * Conventions shared by every call
  * --------------------------------
  * - Every array argument is a DEVICE pointer on the current device, owned and
@@ -283,6 +288,23 @@ bastion_status bastion_kv_commit(const void *k_tree, const void *v_tree, bastion
                                  int Hkv, int d, int K, const int32_t *acc_len, const int32_t *acc_nodes,
                                  const bastion_kv_cache *kv, const int32_t *ctx_len, int32_t *ctx_out,
                                  uint32_t *dev_err, bastion_stream_t stream);
+
+/*
+ * Block-diffusion drafter mask (FlexDraft page, "Attention-Tuning": mask
+ * tokens appended to the clean prefix attend bidirectionally inside their
+ * block and to the clean prefix, isolated from other blocks; BASTION page,
+ * Methodik §1: one drafter pass fills a block of positions).
+ *
+ * Writes mask [B, n_max, ceil(n_max/64)] uint64 for bastion_tree_attn: for
+ * request b and row i < n[b], bit j is set iff j < n[b] and
+ * i / block == j / block; rows i >= n[b] are zero.  With the clean prefix as
+ * the context cache and the block positions' Q/K/V as the tree tensors,
+ * bastion_tree_attn then computes the drafter's attention.  n int32 [B] (device).
+ * Requires 1 <= n_max <= 256, block >= 1.  Device errors: n[b] outside
+ * [1, n_max] (BASTION_DEVERR_N; that request's rows are zero).
+ */
+bastion_status bastion_block_mask(int B, int n_max, int block, const int32_t *n, uint64_t *mask, uint32_t *dev_err,
+                                  bastion_stream_t stream);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -157,3 +157,12 @@ def test_kv_commit_rejects_bad_arguments(L):
     kv.block_table = 16
     kv.max_pages, kv.num_pages, kv.page_size = 0, 8, 16
     assert call() == INVALID
+
+
+def test_block_mask_rejects_bad_arguments(L):
+    f = L.bastion_block_mask
+    assert f(2, 64, 16, None, P, None, None) == INVALID
+    assert f(2, 64, 16, P, None, None, None) == INVALID
+    assert f(0, 64, 16, P, P, None, None) == INVALID
+    assert f(2, 64, 0, P, P, None, None) == INVALID
+    assert f(2, 300, 16, P, P, None, None) == UNSUPPORTED

@@ -58,6 +58,7 @@ _SIGS = {
                                         _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
     "bastion_kv_commit": (_c_int, [_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p,
                                    ctypes.POINTER(KVCache), _c_p, _c_p, _c_p, _c_p]),
+    "bastion_block_mask": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p]),
 }
 
 _lib = None
@@ -314,6 +315,22 @@ def bastion_kv_commit(k_tree, v_tree, kv: "KV", acc_len, acc_nodes, ctx_len, ctx
     _check(lib().bastion_kv_commit(_ptr(k_tree), _ptr(v_tree), _dtype_code(k_tree), B, N, Hkv, d, K, _ptr(acc_len),
                                    _ptr(acc_nodes), ctypes.byref(s), _ptr(ctx_len), _ptr(ctx_out), _ptr(dev_err),
                                    _stream(stream)), "bastion_kv_commit")
+
+
+def bastion_block_mask(n, block: int, mask, dev_err=None, stream=None) -> None:
+    """Block-diffusion drafter mask for bastion_tree_attn: mask int64
+    [B, n_max, ceil(n_max/64)] gets, for row i < n[b], the bits j < n[b] with
+    i // block == j // block; n int32 [B]."""
+    B = n.shape[0]
+    _need(n, torch.int32, (B,), "n")
+    if mask.dim() != 3 or mask.shape[0] != B:
+        raise BastionError("mask must be [B, n_max, ceil(n_max/64)]")
+    N = mask.shape[1]
+    _need(mask, torch.int64, (B, N, (N + 63) // 64), "mask")
+    if dev_err is not None:
+        _need(dev_err, torch.int32, (1,), "dev_err")
+    _check(lib().bastion_block_mask(B, N, int(block), _ptr(n), _ptr(mask), _ptr(dev_err), _stream(stream)),
+           "bastion_block_mask")
 
 
 # --------------------------------------------------------------------------

@@ -51,6 +51,8 @@ cudaError_t launch_kv_commit(const void *k_tree, const void *v_tree, int esz, in
                              const int32_t *acc_len, const int32_t *acc_nodes, void *kc, void *vc, int64_t L_max,
                              const int32_t *block_table, int max_pages, int num_pages, int page_size,
                              const int32_t *ctx_len, int32_t *ctx_out, uint32_t *dev_err, cudaStream_t stream);
+cudaError_t launch_block_mask(int B, int n_max, int block, const int32_t *n, uint64_t *mask, uint32_t *dev_err,
+                              cudaStream_t stream);
 }  // namespace bst
 
 namespace {
@@ -374,6 +376,19 @@ bastion_status bastion_kv_commit(const void *k_tree, const void *v_tree, bastion
                                         kv->block_table, kv->max_pages, kv->num_pages, kv->page_size, ctx_len,
                                         ctx_out, dev_err, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_commit launch");
+  return BASTION_OK;
+}
+
+bastion_status bastion_block_mask(int B, int n_max, int block, const int32_t *n, uint64_t *mask, uint32_t *dev_err,
+                                  bastion_stream_t stream) {
+  if (!n || !mask) return fail(BASTION_ERR_INVALID_ARG, "block_mask: NULL pointer");
+  if (B < 1 || n_max < 1 || block < 1) return fail(BASTION_ERR_INVALID_ARG, "block_mask: bad sizes");
+  if (n_max > BASTION_MAX_NODES || B > 65535) return fail(BASTION_ERR_UNSUPPORTED, "block_mask: n_max <= 256, B <= 65535");
+  int sms = 0;
+  bastion_status s = current_device(&sms);
+  if (s != BASTION_OK) return s;
+  cudaError_t e = bst::launch_block_mask(B, n_max, block, n, mask, dev_err, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "block_mask launch");
   return BASTION_OK;
 }
 
