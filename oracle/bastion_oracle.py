@@ -119,7 +119,7 @@ class Tree:
     min_gap: float          # smallest relative gap of an inexact decision
 
 
-def _build_one(ids, lg, lse, root_tok, ctx_len, n_min, n_max, C, L_AR) -> Tree:
+def _build_one(ids, lg, lse, root_tok, ctx_len, n_min, n_max, C, L_AR, tau=0.0) -> Tree:
     K, k = ids.shape
     # prefix of log-normalisers: P[d] = sum_{t=1..d} lse_t, so that
     # log rho(i) = sum_{t<=d} l_t(x_t) - P[d]   (log of the product in §1)
@@ -180,6 +180,14 @@ def _build_one(ids, lg, lse, root_tok, ctx_len, n_min, n_max, C, L_AR) -> Tree:
         b = best_index()
         min_gap = min(min_gap, decision_gap(b))
         rho_next = math.exp(f_S64[b] - P[f_dep[b]])
+        if tau > 0.0 and n >= n_min:
+            # cumulative draft confidence below the threshold: stop (FlexDraft
+            # page, "Flex-Decoding", selective verification).  Decided on the
+            # fp32 log rho (fp32 logit sum minus the float64 lse prefix, rounded
+            # to fp32) against log tau rounded to fp32.
+            min_gap = min(min_gap, 1.0 - math.exp(-abs(f_key[b] - math.log(tau))))
+            if np.float32(float(f_S[b]) - P[f_dep[b]]) < np.float32(math.log(tau)):
+                break
         if C is not None and n >= n_min:
             s_now = ahat[-1] * L_AR / float(C[n])
             s_next = (ahat[-1] + rho_next) * L_AR / float(C[n + 1])
@@ -226,18 +234,21 @@ def _build_one(ids, lg, lse, root_tok, ctx_len, n_min, n_max, C, L_AR) -> Tree:
 
 
 def tree_build(ids, lg, lse, root_tok, ctx_len, n_min: int, n_max: int,
-               C: Optional[np.ndarray], L_AR: float) -> list:
+               C: Optional[np.ndarray], L_AR: float, tau: float = 0.0) -> list:
     """Best-first tree of every request.
 
     ids/lg are [B, K, k] (top-k of each position, in stage-1 order), lse is
     [B, K].  ``C`` is the latency table C[0..n_max] (entry n is C(n)) or None for
-    a fixed budget (then S(n) is reported with C = 1).  Returns one Tree per
-    request.
+    a fixed budget (then S(n) is reported with C = 1).  ``tau`` > 0 adds the
+    confidence threshold of the FlexDraft page ("Flex-Decoding", selective
+    verification): past n_min the tree also stops at the first node whose
+    rho (the cumulative draft confidence of its path) is below tau.  Returns
+    one Tree per request.
     """
     ids = np.asarray(ids)
     lg = np.asarray(lg, dtype=np.float64)
     lse = np.asarray(lse, dtype=np.float64)
-    return [_build_one(ids[b], lg[b], lse[b], root_tok[b], ctx_len[b], n_min, n_max, C, L_AR)
+    return [_build_one(ids[b], lg[b], lse[b], root_tok[b], ctx_len[b], n_min, n_max, C, L_AR, tau)
             for b in range(ids.shape[0])]
 
 

@@ -76,7 +76,7 @@ def _stage1(logits_bkv):
     return logits_bkv.reshape(B * K, V)
 
 
-def _tree_from_logits(x, k, n_max, n_min=None, C=None, L_AR=1.0, root_tok=None, ctx_len=None):
+def _tree_from_logits(x, k, n_max, n_min=None, C=None, L_AR=1.0, root_tok=None, ctx_len=None, tau=0.0):
     """x [B, K, V] -> (trees, ids, lg, lse) through the oracle's stages 1-2."""
     B, K, V = x.shape
     ids, lg, q, lse = oracle.topk_softmax(x.reshape(B * K, V), k)
@@ -84,7 +84,7 @@ def _tree_from_logits(x, k, n_max, n_min=None, C=None, L_AR=1.0, root_tok=None, 
     root_tok = np.zeros(B, np.int32) if root_tok is None else root_tok
     ctx_len = np.zeros(B, np.int32) if ctx_len is None else ctx_len
     trees = oracle.tree_build(ids, lg, lse, root_tok, ctx_len,
-                              n_max if n_min is None else n_min, n_max, C, L_AR)
+                              n_max if n_min is None else n_min, n_max, C, L_AR, tau)
     return trees, ids, lg, lse
 
 
@@ -543,3 +543,59 @@ def test_one_block_is_unmasked_attention_and_unit_blocks_see_themselves():
         for h in range(Hq):
             np.testing.assert_allclose(solo[0, i, h], vt[0, i, h // 2], rtol=1e-14)
     assert np.all(np.isnan(solo[0, 10:]))
+
+
+# ---------------------------------------------------------------- confidence threshold
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_confidence_threshold_keeps_the_nodes_above_tau(seed):
+    """Without a controller the threshold tree is the prefix of the fixed-budget
+    tree made of its first n_min nodes and every further node with rho >= tau:
+    best-first pops come in non-increasing rho (a child never beats its
+    parent), so the nodes above tau are a prefix."""
+    rng = np.random.default_rng(seed)
+    K, k, V, n_max, n_min = 5, 4, 40, 60, 4
+    x = rng.standard_normal((1, K, V)) * 2
+    full, *_ = _tree_from_logits(x, k, n_max)
+    rho = full[0].rho[:full[0].n]
+    assert np.all(np.diff(rho) <= 1e-12 * rho[:-1])
+    tried = 0
+    for m in range(n_min + 1, len(rho) - 1, 7):
+        if not rho[m - 1] > rho[m] * 1.001:
+            continue
+        tau = math.sqrt(rho[m - 1] * rho[m])   # strictly between node m-1 and node m
+        t, *_ = _tree_from_logits(x, k, n_max, n_min=n_min, tau=tau)
+        assert t[0].n == m == max(n_min, int((rho >= tau).sum()))
+        for f in ("parent", "token", "depth"):
+            assert np.array_equal(getattr(t[0], f)[:m], getattr(full[0], f)[:m]), f
+        tried += 1
+    assert tried >= 3
+    # a threshold above every node leaves n_min nodes; tau = 0 is no threshold
+    t, *_ = _tree_from_logits(x, k, n_max, n_min=n_min, tau=0.999)
+    assert t[0].n == n_min
+    t, *_ = _tree_from_logits(x, k, n_max, n_min=n_min, tau=0.0)
+    assert t[0].n == n_max
+
+
+def test_confidence_threshold_with_controller_stops_at_the_first_rule():
+    """With the S(N) controller as well, the tree stops where the first of the
+    two rules says so: n = min(n under S alone, n under tau alone)."""
+    rng = np.random.default_rng(12)
+    K, k, V, n_max, n_min = 6, 4, 30, 80, 3
+    x = rng.standard_normal((2, K, V)) * 3
+    n_grid = np.arange(n_max + 1, dtype=np.float64)
+    C = (6.0 + 0.04 * n_grid + 0.15 * np.maximum(0, n_grid - 20)).astype(np.float32)
+    s_only, *_ = _tree_from_logits(x, k, n_max, n_min=n_min, C=C)
+    full, *_ = _tree_from_logits(x, k, n_max)
+    tried = 0
+    for b in range(2):
+        rho = full[b].rho[:full[b].n]
+        for m in (n_min + 2, s_only[b].n - 2, s_only[b].n + 5):
+            if not (n_min < m < len(rho) and rho[m - 1] > rho[m] * 1.001):
+                continue
+            tau = math.sqrt(rho[m - 1] * rho[m])
+            both, *_ = _tree_from_logits(x[b:b + 1], k, n_max, n_min=n_min, C=C, tau=tau)
+            assert both[0].n == min(s_only[b].n, m), (b, m)
+            tried += 1
+    assert tried >= 3
