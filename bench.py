@@ -567,6 +567,42 @@ def run_ours(args, rank, world, local_rank):
                    "note": "bastion_block_mask + bastion_tree_attn: B requests x one block of K mask tokens over "
                            "the workload's context (bidirectional inside the block); not part of the step"}
 
+    # ---- beyond the step: stage 2 with the confidence threshold, tau placed
+    # at the rho of the middle node of set 0's first tree; timed alone
+    pruned = None
+    if not args.no_commit:
+        s = sets[0]
+        with torch.cuda.stream(stream):
+            step(*args_of(s))
+        torch.cuda.synchronize()
+        n0 = int(step.n[0].item())
+        tau = float(step.rho[0, max(0, n0 // 2)].item())
+
+        def pruned_once():
+            bn.bastion_tree_build(step.ids, step.lg, step.lse, wl.V, s["root"], s["ctx"], 1, wl.n_max, s["C"],
+                                  s["inp"].L_AR, step.n, step.parent, step.token, step.depth, step.pos, step.rho,
+                                  step.mask, step.ahat, step.S, step.S_curve, dev_err=step.dev_err, stream=stream,
+                                  tau=tau)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                pruned_once()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            torch.cuda._sleep(int(10e6))
+            ev[0].record(stream)
+            for _ in range(100):
+                pruned_once()
+            ev[1].record(stream)
+        torch.cuda.synchronize()
+        assert int(step.dev_err.item()) == 0, "device error word set by the threshold tree build"
+        pruned = {"avg_us": ev[0].elapsed_time(ev[1]) * 1e3 / 100, "tau": tau,
+                  "n": [int(x) for x in step.n.cpu().numpy()],
+                  "note": "bastion_tree_build_threshold on set 0 with n_min = 1 and tau = rho of the middle node "
+                          "of request 0's tree; not part of the step"}
+        with torch.cuda.stream(stream):   # the step's own outputs for set 0 again
+            step(*args_of(s))
+        torch.cuda.synchronize()
+
     # ---- end to end through the public API from pinned host buffers: every
     # step copies its whole input block host -> device and its result block
     # back; the runner keeps two slots so one step's copy overlaps the other's
@@ -620,7 +656,8 @@ def run_ours(args, rank, world, local_rank):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf else "f32",
                 "data": "synthetic", "config": config_of(wl, l2), "roofline": roof, "stages": stages,
-                "cpu_baseline": cpu, "e2e": e2e, "next_rows": {"kv_commit": commit, "drafter_attention": drafter},
+                "cpu_baseline": cpu, "e2e": e2e, "next_rows": {"kv_commit": commit, "drafter_attention": drafter,
+                                                      "tree_build_threshold": pruned},
                 "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk, "tree": {"n": [int(x) for x in nb],
                                         "ahat": [float(x) for x in step.ahat.cpu().numpy()],

@@ -13,8 +13,9 @@
  *                                                                        "baumgestützte Verifizierung")
  *   bastion_accept        greedy (temperature 0) acceptance             (Experimentelle Ergebnisse)
  *
- * and, around the step:
+ * and, beside them:
  *
+ *   bastion_tree_build_threshold  stage 2 with a confidence threshold    (FlexDraft page, "Flex-Decoding")
  *   bastion_kv_commit     the accepted path joins the context KV cache  (FlexDraft page, "Flex-Decoding")
  *   bastion_block_mask    block-diffusion drafter mask for the attention (FlexDraft page, "Attention-Tuning")
  *
@@ -153,6 +154,28 @@ bastion_status bastion_tree_build(const int32_t *ids, const float *lg, const dou
                                   int32_t *depth, int32_t *pos, float *rho, uint64_t *mask,
                                   float *ahat, float *S, float *S_curve, uint32_t *dev_err,
                                   bastion_stream_t stream);
+
+/*
+ * bastion_tree_build with a confidence threshold (FlexDraft page,
+ * "Flex-Decoding", selective verification: branches of low cumulative draft
+ * confidence are pruned and only high-confidence prefixes are verified).
+ *
+ * Arguments and outputs are those of bastion_tree_build plus tau in [0, 1]:
+ * past n_min, the tree also stops at the first node whose rho (the cumulative
+ * draft confidence of its path, the product of its positions' q) is below
+ * tau; with C != NULL whichever of the two stop rules comes first ends the
+ * tree.  The test compares the node's fp32 log rho (fp32 logit sum minus the
+ * float64 lse prefix, rounded to fp32) with log tau rounded to fp32.  Best-first
+ * pops come in non-increasing rho, so without C the tree is the first
+ * max(n_min, #{rho >= tau}) nodes of the fixed-budget tree (capped at n_max).
+ * tau = 0 is bastion_tree_build.  tau outside [0, 1]: BASTION_ERR_INVALID_ARG.
+ */
+bastion_status bastion_tree_build_threshold(const int32_t *ids, const float *lg, const double *lse, int B, int K,
+                                            int k, int V, const int32_t *root_tok, const int32_t *ctx_len, int n_min,
+                                            int n_max, const float *C, float L_AR, float tau, int32_t *n,
+                                            int32_t *parent, int32_t *token, int32_t *depth, int32_t *pos, float *rho,
+                                            uint64_t *mask, float *ahat, float *S, float *S_curve, uint32_t *dev_err,
+                                            bastion_stream_t stream);
 
 /* Context KV cache of the verification attention. */
 typedef struct {

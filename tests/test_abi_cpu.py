@@ -166,3 +166,16 @@ def test_block_mask_rejects_bad_arguments(L):
     assert f(0, 64, 16, P, P, None, None) == INVALID
     assert f(2, 64, 0, P, P, None, None) == INVALID
     assert f(2, 300, 16, P, P, None, None) == UNSUPPORTED
+
+
+def test_tree_build_threshold_rejects_bad_tau(L):
+    f = L.bastion_tree_build_threshold
+
+    def call(tau, ids=P):
+        return f(ids, P, P, 2, 16, 8, 1000, P, P, 8, 64, None, ctypes.c_float(1.0), ctypes.c_float(tau), P, P, P, P,
+                 P, P, P, P, P, None, None, None)
+
+    assert call(0.5, ids=None) == INVALID
+    assert call(-0.1) == INVALID
+    assert call(1.5) == INVALID
+    assert call(float("nan")) == INVALID

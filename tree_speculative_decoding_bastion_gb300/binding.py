@@ -48,6 +48,9 @@ _SIGS = {
     "bastion_tree_build": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_int, _c_int,
                                     _c_p, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                                     _c_p]),
+    "bastion_tree_build_threshold": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p, _c_int,
+                                              _c_int, _c_p, _c_f, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                              _c_p, _c_p, _c_p, _c_p, _c_p]),
     "bastion_tree_attn_workspace_size": (_c_sz, [_c_int, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(KVCache)]),
     "bastion_tree_attn": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f,
                                    ctypes.POINTER(KVCache), _c_p, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p, _c_p]),
@@ -144,9 +147,10 @@ def bastion_topk_softmax(logits: torch.Tensor, k: int, ids, lg, q, lse, dev_err=
 
 def bastion_tree_build(ids, lg, lse, V: int, root_tok, ctx_len, n_min: int, n_max: int, C: Optional[torch.Tensor],
                        L_AR: float, n, parent, token, depth, pos, rho, mask, ahat, S, S_curve=None, dev_err=None,
-                       stream=None) -> None:
+                       stream=None, tau: float = 0.0) -> None:
     """Stage 2. ids int32 / lg float32 [B, K, k]; lse float64 [B, K]; root_tok, ctx_len int32 [B];
-    C float32 [n_max+1] or None (fixed budget). Outputs as in bastion.h."""
+    C float32 [n_max+1] or None (fixed budget); tau > 0 adds the confidence
+    threshold (bastion_tree_build_threshold). Outputs as in bastion.h."""
     B, K, k = ids.shape
     _need(ids, torch.int32, (B, K, k), "ids")
     _need(lg, torch.float32, (B, K, k), "lg")
@@ -167,6 +171,14 @@ def bastion_tree_build(ids, lg, lse, V: int, root_tok, ctx_len, n_min: int, n_ma
         _need(S_curve, torch.float32, (B, n_max), "S_curve")
     if dev_err is not None:
         _need(dev_err, torch.int32, (1,), "dev_err")
+    if tau:
+        _check(lib().bastion_tree_build_threshold(_ptr(ids), _ptr(lg), _ptr(lse), B, K, k, int(V), _ptr(root_tok),
+                                                  _ptr(ctx_len), int(n_min), int(n_max), _ptr(C), float(L_AR),
+                                                  float(tau), _ptr(n), _ptr(parent), _ptr(token), _ptr(depth),
+                                                  _ptr(pos), _ptr(rho), _ptr(mask), _ptr(ahat), _ptr(S),
+                                                  _ptr(S_curve), _ptr(dev_err), _stream(stream)),
+               "bastion_tree_build_threshold")
+        return
     _check(lib().bastion_tree_build(_ptr(ids), _ptr(lg), _ptr(lse), B, K, k, int(V), _ptr(root_tok), _ptr(ctx_len),
                                     int(n_min), int(n_max), _ptr(C), float(L_AR), _ptr(n), _ptr(parent), _ptr(token),
                                     _ptr(depth), _ptr(pos), _ptr(rho), _ptr(mask), _ptr(ahat), _ptr(S),

@@ -23,9 +23,9 @@ cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, 
                                 cudaStream_t stream);
 cudaError_t launch_tree_build(const int32_t *ids, const float *lg, const double *lse, int B, int K, int k, int V,
                               const int32_t *root_tok, const int32_t *ctx_len, int n_min, int n_max, const float *C,
-                              float L_AR, int32_t *n, int32_t *parent, int32_t *token, int32_t *depth, int32_t *pos,
-                              float *rho, uint64_t *mask, float *ahat, float *S, float *S_curve, uint32_t *dev_err,
-                              cudaStream_t stream);
+                              float L_AR, float log_tau, int32_t *n, int32_t *parent, int32_t *token, int32_t *depth,
+                              int32_t *pos, float *rho, uint64_t *mask, float *ahat, float *S, float *S_curve,
+                              uint32_t *dev_err, cudaStream_t stream);
 size_t accept_workspace_size(int B, int n_max);
 cudaError_t launch_accept(const void *target, bool bf16, int B, int n_max, int V, int64_t row_stride, int K,
                           const int32_t *n, const int32_t *parent, const int32_t *token, int32_t *acc_len,
@@ -205,27 +205,50 @@ bastion_status bastion_topk_softmax(const void *logits, bastion_dtype dtype, int
   return BASTION_OK;
 }
 
-bastion_status bastion_tree_build(const int32_t *ids, const float *lg, const double *lse, int B, int K, int k, int V,
-                                  const int32_t *root_tok, const int32_t *ctx_len, int n_min, int n_max,
-                                  const float *C, float L_AR, int32_t *n, int32_t *parent, int32_t *token,
-                                  int32_t *depth, int32_t *pos, float *rho, uint64_t *mask, float *ahat, float *S,
-                                  float *S_curve, uint32_t *dev_err, bastion_stream_t stream) {
+// shared by the two tree-build entry points (tau = 0: no threshold)
+static bastion_status tree_build_impl(const int32_t *ids, const float *lg, const double *lse, int B, int K, int k, int V,
+                               const int32_t *root_tok, const int32_t *ctx_len, int n_min, int n_max, const float *C,
+                               float L_AR, float tau, int32_t *n, int32_t *parent, int32_t *token, int32_t *depth,
+                               int32_t *pos, float *rho, uint64_t *mask, float *ahat, float *S, float *S_curve,
+                               uint32_t *dev_err, bastion_stream_t stream) {
   if (!ids || !lg || !lse || !root_tok || !ctx_len || !n || !parent || !token || !depth || !pos || !rho || !mask ||
       !ahat || !S)
     return fail(BASTION_ERR_INVALID_ARG, "tree_build: NULL pointer");
   if (B < 1 || K < 1 || k < 1 || V < 1 || n_max < 1 || n_min < 1 || n_min > n_max)
     return fail(BASTION_ERR_INVALID_ARG, "tree_build: bad sizes");
   if (!(L_AR > 0.f) || !std::isfinite(L_AR)) return fail(BASTION_ERR_INVALID_ARG, "tree_build: L_AR must be > 0");
+  if (!(tau >= 0.f && tau <= 1.f)) return fail(BASTION_ERR_INVALID_ARG, "tree_build: tau must lie in [0, 1]");
   if (K > BASTION_MAX_DEPTH || k > BASTION_MAX_TOPK || n_max > BASTION_MAX_NODES || V > BASTION_MAX_VOCAB)
     return fail(BASTION_ERR_UNSUPPORTED, "tree_build: K <= 32, k <= 32, n_max <= 256, V <= 262144");
   int sms = 0;
   bastion_status s = current_device(&sms);
   if (s != BASTION_OK) return s;
-  cudaError_t e = bst::launch_tree_build(ids, lg, lse, B, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR, n, parent,
-                                         token, depth, pos, rho, mask, ahat, S, S_curve, dev_err,
+  // log tau in float64, rounded once to the kernel's fp32 comparison precision
+  const float log_tau = tau > 0.f ? static_cast<float>(std::log(static_cast<double>(tau))) : -INFINITY;
+  cudaError_t e = bst::launch_tree_build(ids, lg, lse, B, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR, log_tau,
+                                         n, parent, token, depth, pos, rho, mask, ahat, S, S_curve, dev_err,
                                          reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "tree_build launch");
   return BASTION_OK;
+}
+
+bastion_status bastion_tree_build(const int32_t *ids, const float *lg, const double *lse, int B, int K, int k, int V,
+                                  const int32_t *root_tok, const int32_t *ctx_len, int n_min, int n_max,
+                                  const float *C, float L_AR, int32_t *n, int32_t *parent, int32_t *token,
+                                  int32_t *depth, int32_t *pos, float *rho, uint64_t *mask, float *ahat, float *S,
+                                  float *S_curve, uint32_t *dev_err, bastion_stream_t stream) {
+  return tree_build_impl(ids, lg, lse, B, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR, 0.f, n, parent, token,
+                         depth, pos, rho, mask, ahat, S, S_curve, dev_err, stream);
+}
+
+bastion_status bastion_tree_build_threshold(const int32_t *ids, const float *lg, const double *lse, int B, int K,
+                                            int k, int V, const int32_t *root_tok, const int32_t *ctx_len, int n_min,
+                                            int n_max, const float *C, float L_AR, float tau, int32_t *n,
+                                            int32_t *parent, int32_t *token, int32_t *depth, int32_t *pos, float *rho,
+                                            uint64_t *mask, float *ahat, float *S, float *S_curve, uint32_t *dev_err,
+                                            bastion_stream_t stream) {
+  return tree_build_impl(ids, lg, lse, B, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR, tau, n, parent, token,
+                         depth, pos, rho, mask, ahat, S, S_curve, dev_err, stream);
 }
 
 size_t bastion_tree_attn_workspace_size(int B, int n_max, int Hq, int Hkv, int d, const bastion_kv_cache *kv) {

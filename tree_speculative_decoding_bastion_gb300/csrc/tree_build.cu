@@ -26,7 +26,10 @@
 // the loop has no divergent branch and no warp barrier.  With the controller
 // the pops run until the stop rule can first apply (n_min + 1 nodes) and then
 // in chunks of 8; after each chunk the lanes evaluate rho, A_hat and the
-// S(n+1) < S(n) test in parallel and the first drop ends the tree.
+// S(n+1) < S(n) test in parallel and the first drop ends the tree.  The
+// confidence threshold (FlexDraft page, "Flex-Decoding", selective
+// verification) is a second stop test in the same place: past n_min, a node
+// whose fp32 log rho is below log tau ends the tree.
 // Arithmetic is fp32 except single float64 additions for the lse prefix
 // (this GPU's FP64 pipe is narrow, so no float64 exp/log/division).
 #include <math_constants.h>
@@ -67,7 +70,7 @@ template <int SLOTS>
 __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
     const int32_t *__restrict__ ids_g, const float *__restrict__ lg_g, const double *__restrict__ lse_g,
     int K, int k, int V, const int32_t *__restrict__ root_tok, const int32_t *__restrict__ ctx_len,
-    int n_min, int n_max, const float *__restrict__ Ctab, float L_AR, int32_t *__restrict__ n_out,
+    int n_min, int n_max, const float *__restrict__ Ctab, float L_AR, float log_tau, int32_t *__restrict__ n_out,
     int32_t *__restrict__ parent, int32_t *__restrict__ token, int32_t *__restrict__ depth,
     int32_t *__restrict__ pos, float *__restrict__ rho_out, unsigned long long *__restrict__ mask,
     float *__restrict__ ahat_out, float *__restrict__ S_out, float *__restrict__ S_curve,
@@ -77,6 +80,8 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const bool controller = (Ctab != nullptr);
+  const bool tau_on = log_tau > -CUDART_INF_F;   // confidence threshold (log tau, fp32)
+  const bool eval = controller || tau_on;         // the tree size is decided by a stop rule
 
   if (tid == 0) BST_STAMP(g_k2_trace, 0);
   pdl_wait();
@@ -136,9 +141,9 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
     int n_final = -1;
     int chunk_start = 1;
     while (n_final < 0) {
-      // with the controller, pop until the stop rule can first apply
-      // (n_min + 1 nodes), then test it every 8 pops
-      const int target = controller ? min(n_max, max(n + 8, n_min + 1)) : n_max;
+      // with a stop rule, pop until it can first apply (n_min + 1 nodes),
+      // then test it every 8 pops
+      const int target = eval ? min(n_max, max(n + 8, n_min + 1)) : n_max;
       bool exhausted = false;
       while (n < target) {
         const uint32_t bh = static_cast<uint32_t>(best >> 32);
@@ -184,14 +189,15 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
         ++n;
       }
       __syncwarp();
-      if (controller) {
-        // rho, A_hat and the stop test for the nodes of this chunk, 32 at a time
+      if (eval) {
+        // rho, A_hat and the stop tests for the nodes of this chunk, 32 at a time
         for (int cs = chunk_start; cs < n && n_final < 0; cs += 32) {
           const int j = cs + lane;
           float r = 0.f;
+          float key = 0.f;
           if (j < n) {
             const uint2 nj = sm.NS[j];
-            const float key = static_cast<float>(static_cast<double>(__uint_as_float(nj.x)) - sm.P64[nj.y & 0xFF]);
+            key = static_cast<float>(static_cast<double>(__uint_as_float(nj.x)) - sm.P64[nj.y & 0xFF]);
             r = expf(key);
             sm.rho[j] = r;
           }
@@ -206,8 +212,11 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
           float a_prev = __shfl_up_sync(FULL, a_next, 1);
           if (lane == 0) a_prev = base;                   // A_hat(j)
           if (j < n) sm.ahat[j] = a_next;
-          // tree of size j grows to j + 1 only if S(j + 1) >= S(j)
-          const bool drop = (j < n) && (j >= n_min) && (a_next * Ctab[j] < a_prev * Ctab[j + 1]);
+          // tree of size j grows to j + 1 only if S(j + 1) >= S(j) and node
+          // j's rho (the cumulative draft confidence of its path) is >= tau
+          // (short-circuit order: C is read only for j < n <= n_max)
+          const bool drop = (j < n) && (j >= n_min) &&
+                            ((controller && a_next * Ctab[j] < a_prev * Ctab[j + 1]) || (tau_on && key < log_tau));
           const unsigned dm = __ballot_sync(FULL, drop);
           if (dm) n_final = cs + (__ffs(dm) - 1);
           __syncwarp();
@@ -224,8 +233,8 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
   __syncthreads();
   const int nf = sm.n_final;
 
-  // ---- rho and A_hat for a fixed budget (the controller filled them already)
-  if (!controller) {
+  // ---- rho and A_hat for a fixed budget (a stop rule filled them already)
+  if (!eval) {
     for (int j = 1 + tid; j < nf; j += K2_THREADS) {
       const uint2 nj = sm.NS[j];
       const float key = static_cast<float>(static_cast<double>(__uint_as_float(nj.x)) - sm.P64[nj.y & 0xFF]);
@@ -308,9 +317,9 @@ __global__ void __launch_bounds__(K2_THREADS) tree_build_kernel(
 
 cudaError_t launch_tree_build(const int32_t *ids, const float *lg, const double *lse, int B, int K, int k,
                               int V, const int32_t *root_tok, const int32_t *ctx_len, int n_min, int n_max,
-                              const float *C, float L_AR, int32_t *n, int32_t *parent, int32_t *token,
-                              int32_t *depth, int32_t *pos, float *rho, uint64_t *mask, float *ahat, float *S,
-                              float *S_curve, uint32_t *dev_err, cudaStream_t stream) {
+                              const float *C, float L_AR, float log_tau, int32_t *n, int32_t *parent,
+                              int32_t *token, int32_t *depth, int32_t *pos, float *rho, uint64_t *mask, float *ahat,
+                              float *S, float *S_curve, uint32_t *dev_err, cudaStream_t stream) {
   auto *m = reinterpret_cast<unsigned long long *>(mask);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(B, 1, 1);
@@ -321,7 +330,7 @@ cudaError_t launch_tree_build(const int32_t *ids, const float *lg, const double 
   cfg.numAttrs = fill_launch_attrs(attr);
   // frontier slots per lane: one per 32 nodes of the budget
   auto *fn = n_max <= 64 ? tree_build_kernel<2> : n_max <= 128 ? tree_build_kernel<4> : tree_build_kernel<8>;
-  return cudaLaunchKernelEx(&cfg, fn, ids, lg, lse, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR, n, parent,
+  return cudaLaunchKernelEx(&cfg, fn, ids, lg, lse, K, k, V, root_tok, ctx_len, n_min, n_max, C, L_AR, log_tau, n, parent,
                             token, depth, pos, rho, m, ahat, S, S_curve, dev_err);
 }
 
