@@ -326,8 +326,28 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
 #pragma unroll
         for (int h = 0; h < LY::NH; ++h)
           tma_load_3d(sQ + h * ATT_HALF, &tm_q, &bars->q_full, h * 64, kvh * p.g, b * p.n_max + mtile * (ATT_M / p.g));
-        // one K or V tile (context or tree) into `dst`, completing on `fb`
-        auto load_tile = [&](int j, bool is_v, uint8_t *dst, uint64_t *fb) {
+        // Paged caches: the page ids of a context tile are read from the block
+        // table with all loads in flight together, one K tile ahead of the copy
+        // that needs them, so their latency hides behind the previous tile; the
+        // V copy of a tile reuses the ids its K copy read.  pgB holds the ids of
+        // the last K tile issued, pgA those of the one before, pgN the next.
+        constexpr int MAXPG = ATT_N / 8;          // page_size >= 8
+        constexpr int PG_BEYOND = -2147483647 - 1;   // token past the context: read zeros
+        int pgA[MAXPG], pgB[MAXPG], pgN[MAXPG];
+        auto fetch_pages = [&](int j) {
+          if (!kPaged) return;
+          const int ps = p.page_size;
+#pragma unroll
+          for (int pi = 0; pi < MAXPG; ++pi) {
+            const int tok = (ct0 + j) * ATT_N + pi * ps;
+            pgN[pi] = (j < n_ctx && pi * ps < ATT_N && tok < L)
+                          ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + tok / ps)
+                          : PG_BEYOND;
+          }
+        };
+        // one K or V tile (context or tree) into `dst`, completing on `fb`;
+        // pg: the tile's page ids (paged context tiles)
+        auto load_tile = [&](int j, bool is_v, uint8_t *dst, uint64_t *fb, const int (&pg)[MAXPG]) {
           const CUtensorMap *mc = is_v ? &tm_v : &tm_k;
           const CUtensorMap *mt = is_v ? &tm_vt : &tm_kt;
           if (j < n_ctx) {
@@ -337,15 +357,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
               for (int h = 0; h < LY::NH; ++h) tma_load_3d(dst + h * ATT_HALF, mc, fb, h * 64, ct * ATT_N, b * p.Hkv + kvh);
             } else {
               const int ps = p.page_size;
-              for (int pi = 0; pi < ATT_N / ps; ++pi) {
-                const int tok = ct * ATT_N + pi * ps;
-                int page = p.num_pages;   // out of range: the copy reads zeros
-                if (tok < L) {
-                  page = p.block_table[static_cast<int64_t>(b) * p.max_pages + tok / ps];
-                  if (page < 0 || page >= p.num_pages) {
-                    set_err(p.dev_err, BASTION_DEVERR_PAGE);
-                    page = p.num_pages;
-                  }
+#pragma unroll
+              for (int pi = 0; pi < MAXPG; ++pi) {
+                if (pi * ps >= ATT_N) break;
+                int page = pg[pi];
+                if (page == PG_BEYOND) {
+                  page = p.num_pages;   // out of range: the copy reads zeros
+                } else if (page < 0 || page >= p.num_pages) {
+                  set_err(p.dev_err, BASTION_DEVERR_PAGE);
+                  page = p.num_pages;
                 }
 #pragma unroll
                 for (int h = 0; h < LY::NH; ++h) tma_load_4d(dst + h * ATT_HALF + pi * ps * 128, mc, fb, h * 64, 0, kvh, page);
@@ -363,7 +383,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
           if (j >= ATT_KSTAGES && !mbar_wait(&bars->k_empty[st], ((j / ATT_KSTAGES) - 1) & 1, abort, ATT_WAIT_NS))
             return false;
           mbar_expect_tx(&bars->k_full[st], LY::KV_BYTES);
-          load_tile(j, false, smem + LY::K_OFF + st * LY::KV_BYTES, &bars->k_full[st]);
+          if (kPaged) {
+#pragma unroll
+            for (int pi = 0; pi < MAXPG; ++pi) {
+              pgA[pi] = pgB[pi];
+              pgB[pi] = pgN[pi];
+            }
+            fetch_pages(j + 1);
+          }
+          load_tile(j, false, smem + LY::K_OFF + st * LY::KV_BYTES, &bars->k_full[st], pgB);
           if (j < 8) BST_TRACE_AT(32 + j);
           k_issued = j + 1;
           return true;
@@ -373,12 +401,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
           if (j >= ATT_VSTAGES && !mbar_wait(&bars->v_empty[st], ((j / ATT_VSTAGES) - 1) & 1, abort, ATT_WAIT_NS))
             return false;
           mbar_expect_tx(&bars->v_full[st], LY::KV_BYTES);
-          load_tile(j, true, smem + LY::V_OFF + st * LY::KV_BYTES, &bars->v_full[st]);
+          // V(j) follows K(j + 1) unless j is the last tile
+          load_tile(j, true, smem + LY::V_OFF + st * LY::KV_BYTES, &bars->v_full[st], j + 1 < T ? pgA : pgB);
           if (j < 8) BST_TRACE_AT(48 + j);
           v_issued = j + 1;
           return true;
         };
         // K runs one tile ahead of V
+        fetch_pages(0);
         bool run = issue_k(0);
         for (int j = 0; run && j < T; ++j) {
           if (j + 1 < T && !issue_k(j + 1)) break;
