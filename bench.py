@@ -44,7 +44,7 @@ DEFAULT_WORKLOAD = "qwen3_8b_b1"
 KNOWN_TRAFFIC = {
     ("topk_softmax", "qwen3_8b_b1"): {"bytes": 4899840, "src": "3f36d2757b948f0c"},
     ("tree_build", "qwen3_8b_b1"): {"bytes": 28672, "src": "b1b8d9acb140e26c"},
-    ("tree_attn", "qwen3_8b_b1"): {"bytes": 17638912, "src": "08316a3ae5e79a6d"},
+    ("tree_attn", "qwen3_8b_b1"): {"bytes": 17638400, "src": "db832ca8b3373a81"},
     ("accept", "qwen3_8b_b1"): {"bytes": 19476736, "src": "fa0f3decba794f09"}
 }
 KERNEL_SOURCES = {
