@@ -9,7 +9,9 @@ from .bastion_oracle import (  # noqa: F401
     attend,
     block_mask,
     context_kv,
+    fit_verify_latency,
     kv_commit,
+    latency_table,
     marginals,
     masked_attention,
     path_to_root,

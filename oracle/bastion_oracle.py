@@ -480,3 +480,46 @@ def masked_attention(q, k_tree, v_tree, k_ctx, v_ctx, ctx_len, mask, n, Hkv: int
         values = np.concatenate([vc, np.asarray(v_tree[b, sel, kvh], dtype=np.float64)])
         out[b, i, h] = attend(q[b, i, h], keys, values, scale)
     return out
+
+
+# --------------------------------------------------------------------------
+# Latency-table calibration   ([B] Methodik §3: the controller needs C(N), the
+#          cost of a step that verifies N tree tokens, and L_AR; the pages
+#          model the verification latency from memory bandwidth and compute,
+#          calibrated on observed runtimes of the device)
+# --------------------------------------------------------------------------
+
+KNEE_TIE_RTOL = 1e-9
+
+
+def fit_verify_latency(N, t, knee_lo: int, knee_hi: int):
+    """Least-squares fit of t ≈ a + b N + c max(0, N - knee) for every integer
+    knee in [knee_lo, knee_hi]; returns (a, b, c, knee, sse) of the knee with
+    the smallest squared error (the smallest such knee when several lie within
+    a relative 1e-9 of the minimum).  A knee at or past every N leaves the
+    hinge column zero: that fit is (a, b) alone with c = 0."""
+    N = np.asarray(N, dtype=np.float64)
+    t = np.asarray(t, dtype=np.float64)
+    fits = []
+    for knee in range(knee_lo, knee_hi + 1):
+        hinge = np.maximum(0.0, N - knee)
+        cols = [np.ones_like(N), N] + ([hinge] if np.any(hinge > 0) else [])
+        A = np.stack(cols, axis=1)
+        coef, *_ = np.linalg.lstsq(A, t, rcond=None)
+        r = t - A @ coef
+        a, b = float(coef[0]), float(coef[1])
+        c = float(coef[2]) if len(cols) == 3 else 0.0
+        fits.append((float(r @ r), knee, a, b, c))
+    best = min(f[0] for f in fits)
+    sse, knee, a, b, c = next(f for f in fits if f[0] <= best * (1 + KNEE_TIE_RTOL) + 1e-300)
+    return a, b, c, knee, sse
+
+
+def latency_table(a: float, b: float, c: float, knee: int, t_draft: float, n_max: int):
+    """C[n] = t_draft + a + b n + c max(0, n - knee) for n = 0..n_max (float32,
+    the stage-2 table) and L_AR = T_verify(1) = a + b + c max(0, 1 - knee), the
+    cost of a plain autoregressive step (one token verified)."""
+    n = np.arange(n_max + 1, dtype=np.float64)
+    C = (t_draft + a + b * n + c * np.maximum(0.0, n - knee)).astype(np.float32)
+    L_AR = float(np.float32(a + b + c * max(0.0, 1.0 - knee)))
+    return C, L_AR

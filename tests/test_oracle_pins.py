@@ -599,3 +599,50 @@ def test_confidence_threshold_with_controller_stops_at_the_first_rule():
             assert both[0].n == min(s_only[b].n, m), (b, m)
             tried += 1
     assert tried >= 3
+
+
+# ---------------------------------------------------------------- latency calibration
+
+
+def test_fit_recovers_a_noise_free_piecewise_model():
+    N = np.array([1, 2, 4, 8, 16, 24, 32, 48, 64, 80, 96, 128, 160, 192, 224, 256])
+    for (a, b, c, knee) in ((5.0, 0.03, 0.12, 64), (2.5, 0.0, 0.4, 20), (7.0, 0.05, 0.0, 300)):
+        t = a + b * N + c * np.maximum(0, N - knee)
+        fa, fb, fc, fk, sse = oracle.fit_verify_latency(N, t, 8, 200)
+        assert sse < 1e-18
+        pred = fa + fb * N + fc * np.maximum(0, N - fk)
+        np.testing.assert_allclose(pred, t, rtol=1e-10, atol=1e-12)
+        if c > 0:
+            assert fk == knee and abs(fc - c) < 1e-9 and abs(fb - b) < 1e-9 and abs(fa - a) < 1e-9
+        else:
+            assert abs(fc) < 1e-9   # no hinge in the data: the fitted hinge carries nothing
+
+
+def test_fit_is_the_least_squares_optimum():
+    """Noisy data: at the chosen knee no (a, b, c) fits better (the gradient of
+    the squared error vanishes there), and every other knee's own best fit
+    (solved here from the normal equations) is no better."""
+    rng = np.random.default_rng(3)
+    N = np.arange(1, 257, 5)
+    t = 4.0 + 0.02 * N + 0.3 * np.maximum(0, N - 97) + rng.normal(0, 0.2, N.size)
+    a, b, c, knee, sse = oracle.fit_verify_latency(N, t, 10, 240)
+    X = np.stack([np.ones(N.size), N, np.maximum(0, N - knee)], axis=1).astype(np.float64)
+    r = t - X @ np.array([a, b, c])
+    np.testing.assert_allclose(X.T @ r, 0.0, atol=1e-6)
+    assert abs(sse - r @ r) < 1e-9 * max(1.0, sse)
+    for k in range(10, 241):
+        h = np.maximum(0, N - k).astype(np.float64)
+        Xk = np.stack([np.ones(N.size), N.astype(np.float64)] + ([h] if h.any() else []), axis=1)
+        coef = np.linalg.solve(Xk.T @ Xk, Xk.T @ t)
+        rk = t - Xk @ coef
+        assert rk @ rk >= sse * (1 - 1e-9)
+    assert 90 <= knee <= 105
+
+
+def test_latency_table_closed_form():
+    C, L_AR = oracle.latency_table(3.0, 0.25, 0.5, 10, 1.5, 20)
+    assert C.dtype == np.float32 and C.shape == (21,)
+    assert C[0] == np.float32(4.5) and L_AR == np.float32(3.25)
+    d = np.diff(C.astype(np.float64))
+    np.testing.assert_allclose(d[:10], 0.25, rtol=1e-6)    # n = 1..10: slope b
+    np.testing.assert_allclose(d[10:], 0.75, rtol=1e-6)    # past the knee: b + c
