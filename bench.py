@@ -603,6 +603,22 @@ def run_ours(args, rank, world, local_rank):
             step(*args_of(s))
         torch.cuda.synchronize()
 
+    # ---- beyond the step: calibrate the stage-2 cost table on this device
+    # (the verification attention timed over N, fitted by the library)
+    calib = None
+    if not args.no_commit:
+        from tree_speculative_decoding_bastion_gb300 import calibrate as cal
+        s = sets[0]
+        Ns = sorted({1, *[max(1, (wl.n_max * i) // 8) for i in range(1, 9)]})
+        t_draft = us["topk_softmax"] + us["tree_build"]
+        res = cal.calibrate(s["q"], s["kt"], s["vt"], s["kv"], s["ctx"], s["inp"].scale, Ns, t_draft, reps=20,
+                            stream=stream)
+        calib = {k: res[k] for k in ("Ns", "t_us", "a", "b", "c", "knee", "rms_us", "t_draft_us", "L_AR")}
+        calib["C_n_max"] = float(res["C"][-1].item())
+        calib["note"] = ("T_verify(N) = a + b N + c max(0, N - knee) fitted (microseconds) to the tree attention "
+                         "timed at each N (bastion_fit_verify_latency); C(n) = t_draft + T_verify(n) with t_draft = "
+                         "top-k + tree-build time (bastion_latency_table); not part of the step")
+
     # ---- end to end through the public API from pinned host buffers: every
     # step copies its whole input block host -> device and its result block
     # back; the runner keeps two slots so one step's copy overlaps the other's
@@ -657,7 +673,8 @@ def run_ours(args, rank, world, local_rank):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf else "f32",
                 "data": "synthetic", "config": config_of(wl, l2), "roofline": roof, "stages": stages,
                 "cpu_baseline": cpu, "e2e": e2e, "next_rows": {"kv_commit": commit, "drafter_attention": drafter,
-                                                      "tree_build_threshold": pruned},
+                                                      "tree_build_threshold": pruned,
+                                                      "latency_calibration": calib},
                 "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk, "tree": {"n": [int(x) for x in nb],
                                         "ahat": [float(x) for x in step.ahat.cpu().numpy()],

@@ -18,6 +18,8 @@
  *   bastion_tree_build_threshold  stage 2 with a confidence threshold    (FlexDraft page, "Flex-Decoding")
  *   bastion_kv_commit     the accepted path joins the context KV cache  (FlexDraft page, "Flex-Decoding")
  *   bastion_block_mask    block-diffusion drafter mask for the attention (FlexDraft page, "Attention-Tuning")
+ *   bastion_fit_verify_latency, bastion_latency_table
+ *                         calibration of the stage-2 cost table C(N) (Methodik §3)
  *
  * Conventions shared by every call
  * --------------------------------
@@ -328,6 +330,34 @@ bastion_status bastion_kv_commit(const void *k_tree, const void *v_tree, bastion
  */
 bastion_status bastion_block_mask(int B, int n_max, int block, const int32_t *n, uint64_t *mask, uint32_t *dev_err,
                                   bastion_stream_t stream);
+
+/*
+ * Latency-table calibration (BASTION page, Methodik §3: the controller needs
+ * C(N), the cost of a step that verifies N tree tokens, and L_AR; the pages
+ * model the verification latency from memory bandwidth and compute, calibrated
+ * on the device's observed runtimes).  Host functions: no GPU, no stream.
+ *
+ * bastion_fit_verify_latency: given m >= 3 measured verification times t[i]
+ * (any unit) at tree sizes N[i] (at least two distinct), fits
+ *   T_verify(N) = a + b N + c max(0, N - knee)
+ * by least squares (Householder QR, float64) for every integer knee in
+ * [knee_lo, knee_hi] and returns the knee with the smallest squared error --
+ * the smallest knee among those within 1e-9 of the minimum, relative, or
+ * 1e-12 of sum t^2 -- with abc = {a, b, c} and *sse.  Where the hinge column is
+ * zero or a combination of 1 and N (to 1e-9 of its norm) the fit is the
+ * straight line with c = 0.  Bad input (NULL, m < 3, knee_lo > knee_hi, a
+ * non-finite t, fewer than two distinct N): BASTION_ERR_INVALID_ARG.
+ *
+ * bastion_latency_table: C[n] = t_draft + a + b n + c max(0, n - knee) for
+ * n = 0..n_max (rounded to float: the table bastion_tree_build takes, after
+ * the caller copies it to the device) and *L_AR = a + b + c max(0, 1 - knee),
+ * the cost of verifying one token (a plain autoregressive step).  Requires
+ * 1 <= n_max <= 256.
+ */
+bastion_status bastion_fit_verify_latency(const int32_t *N, const double *t, int m, int knee_lo, int knee_hi,
+                                          double *abc, int32_t *knee, double *sse);
+bastion_status bastion_latency_table(const double *abc, int32_t knee, double t_draft, int n_max, float *C,
+                                     float *L_AR);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -496,22 +496,37 @@ def fit_verify_latency(N, t, knee_lo: int, knee_hi: int):
     """Least-squares fit of t ≈ a + b N + c max(0, N - knee) for every integer
     knee in [knee_lo, knee_hi]; returns (a, b, c, knee, sse) of the knee with
     the smallest squared error (the smallest such knee when several lie within
-    a relative 1e-9 of the minimum).  A knee at or past every N leaves the
-    hinge column zero: that fit is (a, b) alone with c = 0."""
+    1e-9 of the minimum, relative, or 1e-12 of sum t^2).  A knee at or past every N leaves the
+    hinge column zero: that fit is (a, b) alone with c = 0 (as is a knee whose
+    hinge column is a combination of 1 and N).  Needs two distinct N."""
     N = np.asarray(N, dtype=np.float64)
     t = np.asarray(t, dtype=np.float64)
+    if np.unique(N).size < 2:
+        raise ValueError("the fit needs at least two distinct N")
+    line = np.stack([np.ones_like(N), N], axis=1)
     fits = []
     for knee in range(knee_lo, knee_hi + 1):
         hinge = np.maximum(0.0, N - knee)
-        cols = [np.ones_like(N), N] + ([hinge] if np.any(hinge > 0) else [])
+        # the hinge is used only where it is not (to 1e-9 of its norm) a
+        # combination of 1 and N: every N on one side of the knee, or a single
+        # N at the knee, makes the fit a straight line with c = 0
+        use = False
+        if np.any(hinge > 0):
+            proj, *_ = np.linalg.lstsq(line, hinge, rcond=None)
+            use = np.linalg.norm(hinge - line @ proj) > 1e-9 * np.linalg.norm(hinge)
+        cols = [np.ones_like(N), N] + ([hinge] if use else [])
         A = np.stack(cols, axis=1)
         coef, *_ = np.linalg.lstsq(A, t, rcond=None)
         r = t - A @ coef
         a, b = float(coef[0]), float(coef[1])
         c = float(coef[2]) if len(cols) == 3 else 0.0
         fits.append((float(r @ r), knee, a, b, c))
+    # ties: within 1e-9 of the minimum, relative, or 1e-12 of the data's
+    # energy sum t^2 (fits that differ by rounding only, e.g. data without a
+    # hinge, where every knee past the data fits exactly)
     best = min(f[0] for f in fits)
-    sse, knee, a, b, c = next(f for f in fits if f[0] <= best * (1 + KNEE_TIE_RTOL) + 1e-300)
+    tol = best * KNEE_TIE_RTOL + 1e-12 * float(t @ t)
+    sse, knee, a, b, c = next(f for f in fits if f[0] <= best + tol)
     return a, b, c, knee, sse
 
 

@@ -615,7 +615,8 @@ def test_fit_recovers_a_noise_free_piecewise_model():
         if c > 0:
             assert fk == knee and abs(fc - c) < 1e-9 and abs(fb - b) < 1e-9 and abs(fa - a) < 1e-9
         else:
-            assert abs(fc) < 1e-9   # no hinge in the data: the fitted hinge carries nothing
+            # no hinge in the data: every knee fits exactly, the smallest is kept
+            assert abs(fc) < 1e-9 and fk == 8
 
 
 def test_fit_is_the_least_squares_optimum():

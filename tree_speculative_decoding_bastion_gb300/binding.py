@@ -62,6 +62,8 @@ _SIGS = {
     "bastion_kv_commit": (_c_int, [_c_p, _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_p, _c_p,
                                    ctypes.POINTER(KVCache), _c_p, _c_p, _c_p, _c_p]),
     "bastion_block_mask": (_c_int, [_c_int, _c_int, _c_int, _c_p, _c_p, _c_p, _c_p]),
+    "bastion_fit_verify_latency": (_c_int, [_c_p, _c_p, _c_int, _c_int, _c_int, _c_p, _c_p, _c_p]),
+    "bastion_latency_table": (_c_int, [_c_p, ctypes.c_int32, ctypes.c_double, _c_int, _c_p, _c_p]),
 }
 
 _lib = None
@@ -343,6 +345,36 @@ def bastion_block_mask(n, block: int, mask, dev_err=None, stream=None) -> None:
         _need(dev_err, torch.int32, (1,), "dev_err")
     _check(lib().bastion_block_mask(B, N, int(block), _ptr(n), _ptr(mask), _ptr(dev_err), _stream(stream)),
            "bastion_block_mask")
+
+
+def bastion_fit_verify_latency(N, t_us, knee_lo: int, knee_hi: int):
+    """Host fit of T_verify(N) = a + b N + c max(0, N - knee) to measured times
+    (sequences of equal length, at least two distinct N).  Returns
+    (a, b, c, knee, sse)."""
+    import numpy as np
+    N = np.ascontiguousarray(N, dtype=np.int32)
+    t = np.ascontiguousarray(t_us, dtype=np.float64)
+    if N.shape != t.shape or N.ndim != 1:
+        raise BastionError("N and t must be 1-D and of equal length")
+    abc = np.zeros(3, dtype=np.float64)
+    knee = ctypes.c_int32(0)
+    sse = ctypes.c_double(0.0)
+    _check(lib().bastion_fit_verify_latency(N.ctypes.data, t.ctypes.data, int(N.size), int(knee_lo), int(knee_hi),
+                                            abc.ctypes.data, ctypes.byref(knee), ctypes.byref(sse)),
+           "bastion_fit_verify_latency")
+    return float(abc[0]), float(abc[1]), float(abc[2]), int(knee.value), float(sse.value)
+
+
+def bastion_latency_table(a: float, b: float, c: float, knee: int, t_draft: float, n_max: int):
+    """The stage-2 table C[0..n_max] (numpy float32, to be copied to the
+    device) and L_AR = T_verify(1)."""
+    import numpy as np
+    abc = np.array([a, b, c], dtype=np.float64)
+    C = np.zeros(n_max + 1, dtype=np.float32)
+    L_AR = ctypes.c_float(0.0)
+    _check(lib().bastion_latency_table(abc.ctypes.data, int(knee), float(t_draft), int(n_max), C.ctypes.data,
+                                       ctypes.byref(L_AR)), "bastion_latency_table")
+    return C, float(L_AR.value)
 
 
 # --------------------------------------------------------------------------
