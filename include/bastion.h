@@ -82,7 +82,9 @@ typedef enum { BASTION_F32 = 0, BASTION_BF16 = 1 } bastion_dtype;
 #define BASTION_MAX_DEPTH 32    /* K, drafter positions */
 #define BASTION_MAX_VOCAB 262144
 
-/* ABI version of this header (major * 100 + minor). */
+/* ABI version of this header (major * 100 + minor): 101 = 100 plus the calls
+ * beside the step (threshold tree build, KV commit, drafter mask, latency
+ * calibration); the four stage calls are unchanged. */
 int bastion_abi_version(void);
 
 /* Human-readable name of a status. Never NULL. */

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.bastion_abi_version() == 100
+    assert L.bastion_abi_version() == 101
     for s, name in ((OK, b"BASTION_OK"), (INVALID, b"BASTION_ERR_INVALID_ARG"), (WORKSPACE, b"BASTION_ERR_WORKSPACE")):
         assert L.bastion_status_string(s) == name
 

@@ -158,7 +158,7 @@ void set_last_error(const std::string &msg) { g_last = msg; }
 
 extern "C" {
 
-int bastion_abi_version(void) { return 100; }
+int bastion_abi_version(void) { return 101; }
 
 const char *bastion_status_string(bastion_status s) {
   switch (s) {
