@@ -36,11 +36,11 @@ sys.path.insert(0, ROOT)
 from tree_speculative_decoding_bastion_gb300 import inputs as I  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
-DEFAULT_WORKLOAD = "qwen3_8b_b1"
+DEFAULT_WORKLOAD = "long_ctx_b4"
 
-# DRAM bytes (read + write) of one launch, from one ncu capture of the bench's
-# workload (profiles/*.md); an entry counts only while the kernel's sources
-# still hash to `src`
+# DRAM bytes (read + write) of one launch (ncu dram__bytes_read.sum +
+# dram__bytes_write.sum, one capture of the workload); an entry counts only
+# while the kernel's sources still hash to `src`
 KNOWN_TRAFFIC = {
     ("topk_softmax", "qwen3_8b_b1"): {"bytes": 4899840, "src": "3f36d2757b948f0c"},
     ("tree_build", "qwen3_8b_b1"): {"bytes": 28672, "src": "b1b8d9acb140e26c"},
@@ -112,52 +112,204 @@ def job_throughput(world, steps, ms):
     return world * steps / (ms / 1e3)
 
 
-def oracle_sample_step(inp, target, rows_per_request=64, max_requests=1):
-    """Times the oracle's four stages on the first `max_requests` requests
-    (attention on `rows_per_request` (node, head) rows each) and scales each
-    stage to the whole batch.  Returns (seconds per full step, description)."""
+# What the oracle pool's workers read.  Filled in the parent before the pool
+# forks (no GPU call has been made by then), so the workers inherit it.
+_ORACLE = {}
+
+
+def host_cores():
+    """Cores this process may run on (the affinity mask, else the CPU count)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def host_cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+class _F32View:
+    """float32 values of a stored (bf16 bits or float32) array, converted on indexing."""
+
+    def __init__(self, a, dtype):
+        self.a, self.dtype, self.shape = a, dtype, a.shape
+
+    def __getitem__(self, idx):
+        return I.as_f32(self.a[idx], self.dtype)
+
+
+def _w_topk(r0, r1):
     import oracle
-    wl = inp.wl
-    r = min(wl.B, max_requests)
-    f32 = lambda a: I.as_f32(a, wl.dtype)
-    t0 = time.perf_counter()
-    x = f32(inp.logits[:r]).reshape(r * wl.K, wl.V)
-    ids, lg, q, lse = oracle.topk_softmax(x, wl.topk)
-    t1 = time.perf_counter()
-    trees = oracle.tree_build(ids.reshape(r, wl.K, -1), lg.reshape(r, wl.K, -1), lse.reshape(r, wl.K),
-                              inp.root_tok[:r], inp.ctx_len[:r], wl.n_min, wl.n_max, inp.C, inp.L_AR)
-    T = oracle.stack_trees(trees)
-    t2 = time.perf_counter()
-    rng = np.random.default_rng(0)
-    rows = []
-    total_rows = 0
-    for b in range(r):
-        nb = int(T["n"][b])
-        total_rows += nb * wl.Hq
-        cand = [(b, i, h) for i in range(nb) for h in range(wl.Hq)]
-        pick = rng.choice(len(cand), size=min(rows_per_request, len(cand)), replace=False)
-        rows += [cand[j] for j in pick]
+    o = _ORACLE
+    wl = o["wl"]
+    t = time.perf_counter()
+    x = I.as_f32(o["inp"].logits.reshape(wl.B * wl.K, wl.V)[r0:r1], wl.dtype)
+    oracle.topk_softmax(x, wl.topk)
+    return time.perf_counter() - t
 
-    class View:
-        def __init__(self, a):
-            self.a = a
-            self.shape = a.shape
 
-        def __getitem__(self, idx):
-            return f32(self.a[idx])
+def _w_tree(b):
+    import oracle
+    o = _ORACLE
+    wl, inp, s1 = o["wl"], o["inp"], o["s1"]
+    t = time.perf_counter()
+    oracle.tree_build(s1["ids"][b:b + 1], s1["lg"][b:b + 1], s1["lse"][b:b + 1], inp.root_tok[b:b + 1],
+                      inp.ctx_len[b:b + 1], wl.n_min, wl.n_max, inp.C, inp.L_AR)
+    return time.perf_counter() - t
 
-    t3a = time.perf_counter()
-    oracle.tree_attention(View(inp.q), View(inp.k_tree), View(inp.v_tree), View(inp.k_ctx), View(inp.v_ctx),
-                          inp.ctx_len, T["parent"], T["n"], wl.Hkv, inp.scale, block_table=inp.block_table,
+
+def _w_attn(rows):
+    import oracle
+    o = _ORACLE
+    wl, inp, T = o["wl"], o["inp"], o["tree"]
+    v = lambda a: _F32View(a, wl.dtype)
+    t = time.perf_counter()
+    oracle.tree_attention(v(inp.q), v(inp.k_tree), v(inp.v_tree), v(inp.k_ctx), v(inp.v_ctx), inp.ctx_len,
+                          T["parent"], T["n"], wl.Hkv, inp.scale, block_table=inp.block_table,
                           page_size=wl.page_size, rows=rows)
-    t3 = time.perf_counter()
-    oracle.accept(View(target[:r]), T["n"], T["parent"], T["token"], wl.K)
-    t4 = time.perf_counter()
-    scale_b = wl.B / r
-    step = scale_b * ((t1 - t0) + (t2 - t1) + (t4 - t3) + (t3 - t3a) * total_rows / max(1, len(rows)))
-    desc = (f"oracle stages 1,2,4 on {r} of {wl.B} requests and attention on {len(rows)} of {total_rows} "
-            f"(node, head) rows, each stage scaled to the full batch")
-    return step, desc
+    return time.perf_counter() - t
+
+
+def _w_accept(b):
+    import oracle
+    o = _ORACLE
+    wl, T = o["wl"], o["tree"]
+    t = time.perf_counter()
+    oracle.accept(_F32View(o["target"][b:b + 1], wl.dtype), T["n"][b:b + 1], T["parent"][b:b + 1],
+                  T["token"][b:b + 1], wl.K)
+    return time.perf_counter() - t
+
+
+class OracleBench:
+    """The CPU oracle (``oracle/``, numpy float64, as it stands) timed on the
+    host cores over one step of the workload.
+
+    A step runs stages 1, 2 and 4 whole (every drafter row, every request's
+    tree, every tree node's argmax and walk) and stage 3 on a sample: ROWS
+    (node, head) rows from each of up to P (request, KV head) groups, drawn
+    afresh every step.  Attention rows are independent and equally costly
+    within a group, so the step's full time is modelled as the measured wall
+    time of stages 1, 2 and 4 plus the sampled attention's CPU seconds scaled
+    to every row of the batch and spread evenly over the P cores.  The work is
+    spread over P worker processes forked before any GPU call (one BLAS thread
+    each); P = 1 runs it in this process.
+    """
+
+    ROWS = 16
+
+    def __init__(self, wl, inp):
+        import oracle
+        self.wl, self.inp = wl, inp
+        # untimed pre-pass: the oracle's own tree and the target logits for it
+        x = I.as_f32(inp.logits, wl.dtype).reshape(wl.B * wl.K, wl.V)
+        ids, lg, q, lse = oracle.topk_softmax(x, wl.topk)
+        s1 = {"ids": ids.reshape(wl.B, wl.K, -1), "lg": lg.reshape(wl.B, wl.K, -1), "lse": lse.reshape(wl.B, wl.K)}
+        T = oracle.stack_trees(oracle.tree_build(s1["ids"], s1["lg"], s1["lse"], inp.root_tok, inp.ctx_len,
+                                                 wl.n_min, wl.n_max, inp.C, inp.L_AR))
+        target = I.make_target_logits(inp, T["depth"], T["n"])
+        _ORACLE.update(wl=wl, inp=inp, s1=s1, tree=T, target=target)
+        self.T = T
+        self.total_rows = int(sum(int(T["n"][b]) for b in range(wl.B))) * wl.Hq
+        self.groups = [(b, kvh) for b in range(wl.B) for kvh in range(wl.Hkv)]
+        self.pool = None
+        self.P = 1
+        self.count = 0
+
+    def start_pool(self, P):
+        import multiprocessing as mp
+        self.P = max(1, int(P))
+        if self.P > 1:
+            self.pool = mp.get_context("fork").Pool(self.P)
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.terminate()
+            self.pool.join()
+            self.pool = None
+
+    def _sample_rows(self):
+        wl, T = self.wl, self.T
+        rng = np.random.default_rng(self.count)
+        self.count += 1
+        pick = rng.choice(len(self.groups), size=min(self.P, len(self.groups)), replace=False)
+        tasks = []
+        for j in sorted(pick):
+            b, kvh = self.groups[j]
+            nb = int(T["n"][b])
+            cand = [(b, i, kvh * wl.g + h) for i in range(nb) for h in range(wl.g)]
+            sel = rng.choice(len(cand), size=min(self.ROWS, len(cand)), replace=False)
+            tasks.append([cand[k] for k in sorted(sel)])
+        return tasks
+
+    def _map(self, fn, args):
+        if self.pool is None:
+            return [fn(*a) for a in args]
+        return self.pool.starmap(fn, args)
+
+    def step(self):
+        """One timed step; returns (wall seconds, modelled full-step seconds)."""
+        wl = self.wl
+        R = wl.B * wl.K
+        P = self.P
+        cuts = [R * i // P for i in range(P + 1)]
+        tasks = self._sample_rows()
+        t0 = time.perf_counter()
+        self._map(_w_topk, [(cuts[i], cuts[i + 1]) for i in range(P) if cuts[i + 1] > cuts[i]])
+        t1 = time.perf_counter()
+        self._map(_w_tree, [(b,) for b in range(wl.B)])
+        t2 = time.perf_counter()
+        attn = self._map(_w_attn, [(rows,) for rows in tasks])
+        t3 = time.perf_counter()
+        self._map(_w_accept, [(b,) for b in range(wl.B)])
+        t4 = time.perf_counter()
+        sampled = sum(len(r) for r in tasks)
+        attn_full = sum(attn) * self.total_rows / max(1, sampled) / P
+        return t4 - t0, (t1 - t0) + (t2 - t1) + (t4 - t3) + attn_full
+
+    def describe(self):
+        wl = self.wl
+        return (f"per step: oracle stages 1, 2 and 4 on the whole batch ({wl.B * wl.K} drafter rows, {wl.B} trees, "
+                f"{int(self.T['n'].sum())} target rows) and attention on {self.ROWS} (node, head) rows from each of "
+                f"{min(self.P, len(self.groups))} of the {len(self.groups)} (request, KV head) groups "
+                f"({self.total_rows} rows in all); the value is full steps per second under the model: stage 1, 2 "
+                f"and 4 wall time plus the sampled attention's CPU time scaled to every row and spread over "
+                f"{self.P} cores")
+
+
+def time_oracle(wl, inp, steps, warmup, seconds=None):
+    """The oracle on all host cores (forked pool) plus a one-core figure.
+    Must run before this process makes any GPU call.  ``seconds`` (optional)
+    bounds the timed loop instead of ``steps``."""
+    ob = OracleBench(wl, inp)
+    one_wall, one_full = ob.step()           # P = 1, in this process
+    P = host_cores()
+    ob.start_pool(P)
+    try:
+        for _ in range(warmup):
+            ob.step()
+        walls, fulls = [], []
+        t_start = time.perf_counter()
+        while True:
+            w, f = ob.step()
+            walls.append(w)
+            fulls.append(f)
+            if seconds is None and len(walls) >= steps:
+                break
+            if seconds is not None and time.perf_counter() - t_start >= seconds:
+                break
+    finally:
+        ob.close()
+    return {"steps": len(walls), "wall_s": sum(walls), "full_s": sum(fulls), "value": len(fulls) / sum(fulls),
+            "cores": ob.P, "one_core_value": 1.0 / one_full, "one_core_wall_s": one_wall,
+            "sample": ob.describe(), "cpu_model": host_cpu_model()}
 
 
 def run_reference(args, rank, world):
@@ -166,29 +318,17 @@ def run_reference(args, rank, world):
         return
     wl = I.WORKLOADS[args.workload]
     inp = I.make_step_inputs(wl, 0)
-    import oracle
-    x = I.as_f32(inp.logits, wl.dtype).reshape(wl.B * wl.K, wl.V)
-    ids, lg, q, lse = oracle.topk_softmax(x, wl.topk)
-    T = oracle.stack_trees(oracle.tree_build(ids.reshape(wl.B, wl.K, -1), lg.reshape(wl.B, wl.K, -1),
-                                             lse.reshape(wl.B, wl.K), inp.root_tok, inp.ctx_len, wl.n_min,
-                                             wl.n_max, inp.C, inp.L_AR))
-    target = I.make_target_logits(inp, T["depth"], T["n"])
-    steps = max(1, min(args.steps, 3))
-    warm = min(args.warmup, 1)
-    for _ in range(warm):
-        oracle_sample_step(inp, target)
-    times = []
-    desc = ""
-    for _ in range(steps):
-        s, desc = oracle_sample_step(inp, target)
-        times.append(s)
-    sec = sum(times)
-    value = steps / sec
+    r = time_oracle(wl, inp, args.steps, args.warmup)
+    value = r["value"]
+    cpu = {"value": value, "unit": "steps/s", "cores": r["cores"], "kind": "oracle", "sample": r["sample"],
+           "one_core": {"value": r["one_core_value"], "unit": "steps/s", "cores": 1}, "cpu_model": r["cpu_model"]}
     line = {"impl": "reference", "metric": "spec-tree steps/s", "value": value, "unit": "steps/s",
-            "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": 1000.0 * sec / steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(wl, "oracle on host cores"),
-            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * r["wall_s"] / r["steps"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, "oracle on host cores"), "cpu_baseline": cpu,
+            "value_model": "value = timed steps / modelled full-step seconds (stages 1, 2, 4 measured whole, "
+                           "attention scaled from a row sample); ms_per_step = measured wall time per timed step",
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -296,15 +436,34 @@ def attn_flops(wl, inp, n, depth):
     return f
 
 
+def tree_report(step):
+    """Per request of the last step run: the chosen tree size n, A_hat(T_n),
+    S(n), the accepted length and the tokens the step emits (accepted + bonus)."""
+    acc = [int(x) for x in step.acc_len.cpu().numpy()]
+    return {"n": [int(x) for x in step.n.cpu().numpy()], "ahat": [float(x) for x in step.ahat.cpu().numpy()],
+            "S": [float(x) for x in step.S.cpu().numpy()], "acc_len": acc, "tokens_per_step": [a + 1 for a in acc],
+            "mean_tokens_per_step": sum(a + 1 for a in acc) / len(acc)}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from tree_speculative_decoding_bastion_gb300 import binding as bn
     from tree_speculative_decoding_bastion_gb300 import build
 
     build.build()
+    wl = I.WORKLOADS[args.workload]
+    first_set = I.make_step_inputs(wl, replica_seed(rank, 0))
+    # ---- CPU baseline: the oracle on the host cores (rank 0, one GPU only),
+    # before this process makes any GPU call (its worker pool is forked)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_oracle(wl, first_set, 1, 1, seconds=args.cpu_seconds)
+        cpu = {"value": r["value"], "unit": "steps/s", "cores": r["cores"], "kind": "oracle",
+               "sample": r["sample"] + f"; {r['steps']} timed steps ({r['wall_s']:.1f} s)",
+               "one_core": {"value": r["one_core_value"], "unit": "steps/s", "cores": 1},
+               "cpu_model": r["cpu_model"]}
     torch.cuda.set_device(local_rank)
     bn.bastion_init(local_rank)
-    wl = I.WORKLOADS[args.workload]
     dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     hbm, tf_burst, tf_sust, peak_kind = peaks()
 
@@ -321,7 +480,7 @@ def run_ours(args, rank, world, local_rank):
     n_sets = args.sets
     r = 0
     while True:
-        inp = I.make_step_inputs(wl, replica_seed(rank, r))
+        inp = first_set if r == 0 else I.make_step_inputs(wl, replica_seed(rank, r))
         s = dict(inp=inp, logits=up(inp.logits, bf), root=up(inp.root_tok), ctx=up(inp.ctx_len),
                  C=None if inp.C is None else up(inp.C), q=up(inp.q, bf), kt=up(inp.k_tree, bf),
                  vt=up(inp.v_tree, bf))
@@ -651,20 +810,6 @@ def run_ours(args, rank, world, local_rank):
                        "(one CUDA graph), one D2H copy of n, accepted length/tokens and bonus; the host waits for "
                        "each result. The context KV cache is resident model state"}
 
-    # ---- CPU baseline: the oracle on a bounded sample (rank 0, one GPU only)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        s = sets[0]
-        target_np = I.make_target_logits(s["inp"], step.depth.cpu().numpy(), step.n.cpu().numpy())
-        times = []
-        desc = ""
-        t_start = time.perf_counter()
-        while time.perf_counter() - t_start < args.cpu_seconds or not times:
-            t, desc = oracle_sample_step(s["inp"], target_np)
-            times.append(t)
-        cpu = {"value": len(times) / sum(times), "unit": "steps/s", "cores": 1, "kind": "oracle",
-               "sample": desc + f"; {len(times)} samples"}
-
     if rank == 0:
         value = job_throughput(world, args.steps, ms)
         l2 = f"rotating {len(sets)} input sets of {set_bytes / 1e6:.1f} MB (> 2x L2)"
@@ -676,9 +821,7 @@ def run_ours(args, rank, world, local_rank):
                                                       "tree_build_threshold": pruned,
                                                       "latency_calibration": calib},
                 "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk, "tree": {"n": [int(x) for x in nb],
-                                        "ahat": [float(x) for x in step.ahat.cpu().numpy()],
-                                        "acc_len": [int(x) for x in step.acc_len.cpu().numpy()]},
+                "clocks": clk, "tree": tree_report(step),
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
         print(json.dumps(line), flush=True)
 
@@ -686,7 +829,7 @@ def run_ours(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40000)   # about 2 s timed: the clock sampler sees the region
+    ap.add_argument("--steps", type=int, default=5000)   # about 2 s timed on long_ctx_b4: the clock sampler sees it
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))

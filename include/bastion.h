@@ -64,7 +64,9 @@ typedef enum {
   BASTION_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels handle */
   BASTION_ERR_WORKSPACE = 3,    /* workspace smaller than the *_workspace_size() */
   BASTION_ERR_CUDA = 4,         /* a CUDA runtime/driver call or launch failed */
-  BASTION_ERR_NO_DEVICE = 5     /* no usable sm_103 device */
+  BASTION_ERR_NO_DEVICE = 5,    /* no usable sm_103 device */
+  BASTION_ERR_DEVICE = 6,       /* the device error word reports bad data (bastion_error_status) */
+  BASTION_ERR_TIMEOUT = 7       /* the device error word reports an expired in-kernel wait */
 } bastion_status;
 
 typedef enum { BASTION_F32 = 0, BASTION_BF16 = 1 } bastion_dtype;
@@ -84,11 +86,32 @@ typedef enum { BASTION_F32 = 0, BASTION_BF16 = 1 } bastion_dtype;
 
 /* ABI version of this header (major * 100 + minor): 101 = 100 plus the calls
  * beside the step (threshold tree build, KV commit, drafter mask, latency
- * calibration); the four stage calls are unchanged. */
+ * calibration); 102 = 101 plus the error-word helpers (bastion_read_error,
+ * bastion_error_status, BASTION_ERR_DEVICE / _TIMEOUT), bastion_status_str and
+ * bastion_topk_softmax_workspace_size; the four stage calls are unchanged. */
 int bastion_abi_version(void);
 
-/* Human-readable name of a status. Never NULL. */
+/* Human-readable name of a status. Never NULL.  bastion_status_str is the
+ * same function under a shorter name. */
 const char *bastion_status_string(bastion_status s);
+const char *bastion_status_str(bastion_status s);
+
+/* Device error word helpers.  Every call takes an optional device pointer
+ * dev_err to one uint32 that the kernels OR BASTION_DEVERR_* bits into; the
+ * caller zeroes it (e.g. cudaMemsetAsync) and reads it after the work is done.
+ *
+ * bastion_read_error enqueues on `stream` an asynchronous copy of the word at
+ * dev_err (device) to *host_word (host; pinned memory keeps the copy
+ * asynchronous) and returns at once; *host_word is valid once the caller has
+ * synchronised with the stream.  NULL pointers: BASTION_ERR_INVALID_ARG; a
+ * failed copy: BASTION_ERR_CUDA.
+ *
+ * bastion_error_status maps a word to a status: 0 -> BASTION_OK; the
+ * BASTION_DEVERR_TIMEOUT bit -> BASTION_ERR_TIMEOUT (the outputs of the call
+ * that set it are invalid); any other bit -> BASTION_ERR_DEVICE (some request
+ * had bad data and was skipped as documented per call). */
+bastion_status bastion_read_error(const uint32_t *dev_err, uint32_t *host_word, bastion_stream_t stream);
+bastion_status bastion_error_status(uint32_t word);
 
 /* Explanation of the last error status returned on this host thread
  * (empty string if none). */
@@ -118,6 +141,11 @@ bastion_status bastion_init(int device);
  * row_stride >= V.  Logits must be finite.  No workspace.  dev_err (nullable)
  * receives BASTION_DEVERR_TIMEOUT if a staged copy of the row never landed.
  */
+/* Workspace bytes bastion_topk_softmax needs: always 0 (the partial results
+ * of a row's CTAs meet in distributed shared memory inside one thread-block
+ * cluster, so the call takes no workspace argument). */
+size_t bastion_topk_softmax_workspace_size(int rows, int V, int k);
+
 bastion_status bastion_topk_softmax(const void *logits, bastion_dtype dtype, int rows, int V,
                                     int64_t row_stride, int k, int32_t *ids, float *lg, float *q,
                                     double *lse, uint32_t *dev_err, bastion_stream_t stream);
@@ -271,9 +299,11 @@ bastion_status bastion_accept(const void *target, bastion_dtype dtype, int B, in
  * Arguments, layouts, results and device-error behaviour are those of
  * bastion_accept.  Sizes whose scratch (bastion_accept_workspace_size(B, n_max))
  * exceeds the array return BASTION_ERR_UNSUPPORTED with an explanation in
- * bastion_last_error().  The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress) with that device current; make that
- * first call (or bastion_init) before any stream capture.  Each call clears
+ * bastion_last_error().  The array's device address is looked up
+ * (cudaGetSymbolAddress) once per device, with that device current, while
+ * bastion_init prepares the device -- which the first call of this library on
+ * a device (this one included) runs implicitly; make that first call, or
+ * bastion_init, before any stream capture.  Each call clears
  * the ticket words on `stream`, then launches.  All calls share the one array:
  * calls that overlap on the GPU (different streams, or different host
  * threads, without ordering between them) race and give wrong results.

@@ -13,7 +13,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "bastion.h")
 
-OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA, NO_DEVICE = 0, 1, 2, 3, 4, 5
+OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA, NO_DEVICE, DEVICE, TIMEOUT = 0, 1, 2, 3, 4, 5, 6, 7
 
 
 @pytest.fixture(scope="module")
@@ -41,9 +41,24 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.bastion_abi_version() == 101
-    for s, name in ((OK, b"BASTION_OK"), (INVALID, b"BASTION_ERR_INVALID_ARG"), (WORKSPACE, b"BASTION_ERR_WORKSPACE")):
+    assert L.bastion_abi_version() == 102
+    for s, name in ((OK, b"BASTION_OK"), (INVALID, b"BASTION_ERR_INVALID_ARG"), (WORKSPACE, b"BASTION_ERR_WORKSPACE"),
+                    (DEVICE, b"BASTION_ERR_DEVICE"), (TIMEOUT, b"BASTION_ERR_TIMEOUT")):
         assert L.bastion_status_string(s) == name
+        assert L.bastion_status_str(s) == name
+
+
+def test_error_word_helpers(L):
+    from tree_speculative_decoding_bastion_gb300 import binding as bn
+    assert L.bastion_error_status(0) == OK
+    for bit in (bn.DEVERR_TOKEN, bn.DEVERR_N, bn.DEVERR_CTX, bn.DEVERR_PAGE):
+        assert L.bastion_error_status(bit) == DEVICE
+    assert L.bastion_error_status(bn.DEVERR_TIMEOUT) == TIMEOUT
+    assert L.bastion_error_status(bn.DEVERR_TIMEOUT | bn.DEVERR_N) == TIMEOUT
+    # NULL pointers are refused before any copy is enqueued
+    assert L.bastion_read_error(None, ctypes.c_void_p(16), None) == INVALID
+    assert L.bastion_read_error(ctypes.c_void_p(16), None, None) == INVALID
+    assert L.bastion_topk_softmax_workspace_size(64, 151936, 8) == 0
 
 
 P = ctypes.c_void_p(16)   # a non-NULL dummy; never dereferenced on these paths

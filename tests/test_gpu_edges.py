@@ -225,3 +225,64 @@ def test_accept_invalid_n_sets_error_bit_and_fills_minus_one():
                          token[:1].cpu().numpy(), K)
     assert int(out["len"][0].item()) == int(want[0][0])
     assert int(out["bonus"][0].item()) == int(want[3][0])
+
+
+# --------------------------------------------------------------------------
+# signed zeros: -0.0 and +0.0 are equal values, so ties between them go to
+# the lower id, as in the oracle (a float comparison, not a bit comparison)
+# --------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_accept_argmax_ties_between_signed_zeros(dtype):
+    """Rows whose maximum is zero, held as -0.0 and +0.0 at different ids: in
+    different CTAs (chunks), in different threads of one CTA, in the same
+    16-byte vector, and with +0.0 first.  The argmax is the lowest id of
+    either sign, as np.argmax gives."""
+    B, N, V, K = 1, 6, 151936, 4
+    rows = np.full((B, N, V), -1.0, np.float32)
+    zeros = {0: [(100, -0.0), (100000, 0.0)],     # chunk 0 vs a later chunk
+             1: [(50, 0.0), (60, -0.0)],          # +0.0 first
+             2: [(8, -0.0), (3000, 0.0)],         # two threads of one CTA
+             3: [(3, -0.0), (2, 0.0)],            # one 16-byte vector, +0.0 lower
+             4: [(40000, -0.0), (30000, -0.0), (151935, 0.0)],
+             5: [(7, 0.0)]}
+    for i, zs in zeros.items():
+        for j, z in zs:
+            rows[0, i, j] = z
+    stored = I.store(rows, dtype)
+    target = C.dev(stored, dtype)
+    n = torch.tensor([N], dtype=torch.int32, device="cuda")
+    parent_h = np.array([[-1, 0, 0, 1, 1, 2]], np.int32)
+    token_h = np.array([[5, 100, 50, 8, 2, 3]], np.int32)
+    parent, token = C.dev(parent_h), C.dev(token_h)
+    out = {k: torch.full(s, -7, dtype=torch.int32, device="cuda")
+           for k, s in (("len", (B,)), ("nodes", (B, K + 1)), ("tok", (B, K + 1)), ("bonus", (B,)), ("am", (B, N)))}
+    ws = torch.zeros(bn.bastion_accept_workspace_size(B, N), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bn.bastion_accept(target, n, parent, token, K, out["len"], out["nodes"], out["tok"], out["bonus"], ws,
+                      argmax_out=out["am"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want = oracle.accept(C.fview(stored, dtype), np.array([N]), parent_h, token_h, K)
+    assert list(want[4][0]) == [100, 50, 8, 2, 30000, 7]
+    for k_, wv in zip(("len", "nodes", "tok", "bonus", "am"), want):
+        assert np.array_equal(out[k_].cpu().numpy(), wv), k_
+
+
+def test_topk_ties_between_signed_zeros():
+    """Every logit zero, even ids -0.0 and odd ids +0.0: all are equal, so the
+    top-k is ids 0..k-1 (through the exact-selection path for massive ties),
+    the logits come back with their own signs, and the tree matches the
+    oracle's."""
+    wl = W["qwen3_8b_b1"].scaled(name="signed_zero", B=2, V=50000, K=4, topk=5, n_min=30, n_max=30, L=16)
+    inp = I.make_step_inputs(wl, 0, with_attention=False)
+    z = np.zeros(wl.V, np.float32)
+    z[0::2] = -0.0
+    inp.logits[...] = I.to_bf16_bits(z)
+    o = C.oracle_draft(inp)
+    s1, tree = run_draft(inp)
+    check_stage1(wl, s1, o)
+    assert (s1["ids"][..., :5] == np.arange(5)).all()
+    assert np.array_equal(np.signbit(s1["lg"].reshape(-1, 5)), np.signbit(o["lg"]))
+    check_tree(tree, o["tree"])

@@ -5,8 +5,9 @@ memory is planned once at start-up), so they cannot provide the workspace
 that bastion_accept takes.  bastion_accept_noalloc keeps that scratch in a
 fixed array inside the library.  This file checks, through the C ABI, that it
 returns exactly what bastion_accept returns, on two calls in a row (the
-shared scratch must not carry state from one call into the next), and that
-sizes beyond its fixed array are refused.  It is collected last on purpose.
+shared scratch must not carry state from one call into the next), that both
+agree with the CPU oracle, and that sizes beyond its fixed array are refused.
+It is collected last on purpose.
 """
 import ctypes
 
@@ -36,18 +37,25 @@ def _outputs(B, N, K):
                          ("argmax", (B, N)))}
 
 
-def _case(name, seed):
-    wl = I.WORKLOADS["controller_sweep_peaked"].scaled(name=name, B=4, V=30011, n_min=1, n_max=48, L=64)
+def _case(name, seed, V):
+    wl = I.WORKLOADS["controller_sweep_peaked"].scaled(name=name, B=4, V=V, n_min=1, n_max=48, L=64)
     inp, o = C.pick(wl, seed, with_attention=False)
     tree = o["tree"]
-    target = C.dev(C.target_for(inp, tree), wl.dtype)
-    return wl, tree, target
+    target_h = C.target_for(inp, tree)
+    want = C.oracle_accept(inp, tree, target_h)
+    return wl, tree, C.dev(target_h, wl.dtype), want
+
+
+# V = 30011: a bf16 row is not a multiple of 16 bytes, so the kernel reads it
+# with plain loads; V = 30016: 16-byte rows, staged with bulk copies (the form
+# the Qwen3- and Llama-sized vocabularies take)
+CASES = (("noalloc_scalar", 0, 30011), ("noalloc_bulk", 1, 30016))
 
 
 def test_noalloc_accept_matches_workspace_accept_twice_in_a_row():
-    cases = [_case("noalloc_a", 0), _case("noalloc_b", 1)]
+    cases = [_case(*c) for c in CASES]
     for rep in range(2):
-        for wl, tree, target in cases:
+        for wl, tree, target, want in cases:
             B, N, K = wl.B, wl.n_max, wl.K
             n, par, tok = C.dev(tree["n"]), C.dev(tree["parent"]), C.dev(tree["token"])
             ref = _outputs(B, N, K)
@@ -60,8 +68,10 @@ def test_noalloc_accept_matches_workspace_accept_twice_in_a_row():
                                       got["bonus"], argmax_out=got["argmax"], dev_err=err)
             torch.cuda.synchronize()
             assert int(err.item()) == 0
-            for k in ref:   # integer outputs: exact
+            for k in ref:   # integer outputs: exact, against the workspace call and against the oracle
                 assert torch.equal(got[k], ref[k]), (rep, wl.name, k)
+            for k, wv in zip(("acc_len", "acc_nodes", "acc_tok", "bonus", "argmax"), want):
+                assert np.array_equal(got[k].cpu().numpy(), wv), (rep, wl.name, k)
 
 
 def test_noalloc_accept_refuses_sizes_beyond_its_array():

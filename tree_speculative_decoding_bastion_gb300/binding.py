@@ -41,6 +41,10 @@ class KVCache(ctypes.Structure):
 _SIGS = {
     "bastion_abi_version": (_c_int, []),
     "bastion_status_string": (ctypes.c_char_p, [_c_int]),
+    "bastion_status_str": (ctypes.c_char_p, [_c_int]),
+    "bastion_read_error": (_c_int, [_c_p, _c_p, _c_p]),
+    "bastion_error_status": (_c_int, [ctypes.c_uint32]),
+    "bastion_topk_softmax_workspace_size": (_c_sz, [_c_int, _c_int, _c_int]),
     "bastion_last_error": (ctypes.c_char_p, []),
     "bastion_init": (_c_int, [_c_int]),
     "bastion_topk_softmax": (_c_int, [_c_p, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p,
@@ -122,6 +126,24 @@ def _need(t: torch.Tensor, dtype, shape, name: str) -> None:
 
 def bastion_init(device: int = 0) -> None:
     _check(lib().bastion_init(int(device)), "bastion_init")
+
+
+def bastion_read_error(dev_err: torch.Tensor, stream=None) -> int:
+    """The device error word (int32/uint32 [1] on the device): the library
+    enqueues the copy on `stream`, this helper then waits for that stream and
+    returns the word (BASTION_DEVERR_* bits)."""
+    _need(dev_err, None, (1,), "dev_err")
+    host = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(lib().bastion_read_error(_ptr(dev_err), ctypes.c_void_p(host.data_ptr()), ctypes.c_void_p(s.cuda_stream)),
+           "bastion_read_error")
+    s.synchronize()
+    return int(host.item()) & 0xFFFFFFFF
+
+
+def bastion_error_status(word: int) -> int:
+    """Status of an error word: 0 OK, 6 bad data, 7 an in-kernel wait expired."""
+    return int(lib().bastion_error_status(int(word) & 0xFFFFFFFF))
 
 
 def bastion_topk_softmax(logits: torch.Tensor, k: int, ids, lg, q, lse, dev_err=None, stream=None) -> None:

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
   __shared__ uint64_t s_bar;
   __shared__ unsigned long long s_red[K4_WARPS];
   __shared__ int s_last;
+  __shared__ int s_dead;   // a staged copy never landed: issue no further copies
   __shared__ int32_t s_am[BASTION_MAX_NODES], s_par[BASTION_MAX_NODES], s_tok[BASTION_MAX_NODES];
 
   // CTA (crank, b, z) takes chunk crank of the rows z, z + Y, ... of request b
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
   const int len = max(0, c1 - c0);
   if (tid == 0) BST_STAMP(g_k4_trace, 0);
   if (kBulk && tid == 0) {
+    s_dead = 0;
     mbar_init(&s_bar, 1);
     fence_mbar_init();
     // warm L2 with the first chunk while the producing grid finishes
@@ -103,6 +105,7 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
     }
   };
   int it = 0;
+  int dead_it = -1;   // the row whose staged copy timed out (kBulk)
   for (int i = z; i < nb; i += Y, ++it) {
     const int row = b * n_max + i;
     const T *rowp = req + static_cast<int64_t>(i) * row_stride;
@@ -111,7 +114,10 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
     if (kBulk) {
       // ---- stage the chunk into shared memory with bulk copies
       const uint32_t bytes = static_cast<uint32_t>(len) * sizeof(T);
-      if (tid == 0 && bytes > 0) {
+      // s_dead was last written before the previous row's barrier, so every
+      // thread reads the same value here
+      const bool dead = s_dead != 0;
+      if (tid == 0 && bytes > 0 && !dead) {
         mbar_expect_tx(&s_bar, bytes);
         for (uint32_t off = 0; off < bytes; off += 16384u) {
           const uint32_t nbytes = min(16384u, bytes - off);
@@ -122,8 +128,14 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
       }
       if (it == 0) stage_tree();   // while the first chunk is in flight
       int no_abort = 0;
-      if (bytes > 0 && !mbar_wait(&s_bar, it & 1, &no_abort, K4_WAIT_NS)) {
-        if (tid == 0) set_err(dev_err, BASTION_DEVERR_TIMEOUT);
+      if (dead) {
+        // an earlier copy of this CTA never landed: the row counts as empty
+        // (its ticket is still taken, so the request completes and the
+        // workspace returns to zero)
+      } else if (bytes > 0 && !mbar_wait(&s_bar, it & 1, &no_abort, K4_WAIT_NS)) {
+        s_dead = 1;
+        dead_it = it;
+        set_err(dev_err, BASTION_DEVERR_TIMEOUT);
       } else {
         // thread t scans 16-byte vectors t, t + 256, ... in increasing order, so
         // a strict ">" keeps its first maximum
@@ -168,6 +180,12 @@ __global__ void __launch_bounds__(K4_THREADS) accept_kernel(
     }
     __syncthreads();
     if (s_last) break;   // every (row, chunk) of the request is in: no row remains
+  }
+  if (kBulk && dead_it >= 0) {
+    // let the copy that timed out land (bounded) before this CTA's shared
+    // memory can go to another CTA
+    int no_abort = 0;
+    mbar_wait(&s_bar, dead_it & 1, &no_abort, K4_WAIT_NS);
   }
   if (!s_last) return;
 

@@ -47,6 +47,23 @@ bastion_status noalloc_fail(bastion_status s, const std::string &m) {
 
 }  // namespace
 
+namespace bst {
+// Set-up of `dev`, once per device, with `dev` current (bastion_init runs it
+// while it prepares the device, so the first library call on a device does
+// it): the host-side name of the array is not a device address, so look the
+// address up.  A failure is kept and reported by bastion_accept_noalloc.
+void prepare_accept_noalloc(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return;
+  ScratchState &st = g_scratch[dev];
+  std::call_once(st.once, [&] {
+    st.err = cudaGetSymbolAddress(&st.ptr, g_accept_scratch);
+    cudaDeviceProp prop;
+    if (st.err == cudaSuccess) st.err = cudaGetDeviceProperties(&prop, dev);
+    if (st.err == cudaSuccess) st.sms = prop.multiProcessorCount;
+  });
+}
+}  // namespace bst
+
 extern "C" bastion_status bastion_accept_noalloc(const void *target, bastion_dtype dtype, int B, int n_max, int V,
                                                  int64_t row_stride, int K, const int32_t *n,
                                                  const int32_t *parent, const int32_t *token, int32_t *acc_len,
@@ -70,17 +87,11 @@ extern "C" bastion_status bastion_accept_noalloc(const void *target, bastion_dty
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return noalloc_fail(BASTION_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return noalloc_fail(BASTION_ERR_NO_DEVICE, "accept_noalloc: device index too large");
+  // bastion_init prepares the device, the scratch address included
   bastion_status s = bastion_init(dev);
   if (s != BASTION_OK) return s;   // bastion_init already recorded why
-  // Set-up, once per device, with that device current: the host-side name of
-  // the array is not a device address, so look the address up.
   ScratchState &st = g_scratch[dev];
-  std::call_once(st.once, [&] {
-    st.err = cudaGetSymbolAddress(&st.ptr, g_accept_scratch);
-    cudaDeviceProp prop;
-    if (st.err == cudaSuccess) st.err = cudaGetDeviceProperties(&prop, dev);
-    if (st.err == cudaSuccess) st.sms = prop.multiProcessorCount;
-  });
+  bst::prepare_accept_noalloc(dev);   // no-op once done
   if (st.err != cudaSuccess || !st.ptr)
     return noalloc_fail(BASTION_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(st.err));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

@@ -53,6 +53,7 @@ cudaError_t launch_kv_commit(const void *k_tree, const void *v_tree, int esz, in
                              const int32_t *ctx_len, int32_t *ctx_out, uint32_t *dev_err, cudaStream_t stream);
 cudaError_t launch_block_mask(int B, int n_max, int block, const int32_t *n, uint64_t *mask, uint32_t *dev_err,
                               cudaStream_t stream);
+void prepare_accept_noalloc(int dev);
 }  // namespace bst
 
 namespace {
@@ -101,6 +102,7 @@ void init_device(int device, DeviceState &st) {
   cudaError_t e2 = bst::prepare_accept();
   cudaError_t e3 = bst::prepare_tree_attn();
   cudaError_t e4 = bst::prepare_tree_build();
+  bst::prepare_accept_noalloc(device);   // the built-in acceptance scratch's address on this device
   if (prev >= 0) cudaSetDevice(prev);
   const cudaError_t ea = e1 != cudaSuccess ? e1 : e2 != cudaSuccess ? e2 : e3 != cudaSuccess ? e3 : e4;
   if (ea != cudaSuccess) {
@@ -158,7 +160,7 @@ void set_last_error(const std::string &msg) { g_last = msg; }
 
 extern "C" {
 
-int bastion_abi_version(void) { return 101; }
+int bastion_abi_version(void) { return 102; }
 
 const char *bastion_status_string(bastion_status s) {
   switch (s) {
@@ -168,8 +170,33 @@ const char *bastion_status_string(bastion_status s) {
     case BASTION_ERR_WORKSPACE: return "BASTION_ERR_WORKSPACE";
     case BASTION_ERR_CUDA: return "BASTION_ERR_CUDA";
     case BASTION_ERR_NO_DEVICE: return "BASTION_ERR_NO_DEVICE";
+    case BASTION_ERR_DEVICE: return "BASTION_ERR_DEVICE";
+    case BASTION_ERR_TIMEOUT: return "BASTION_ERR_TIMEOUT";
   }
   return "BASTION_ERR_UNKNOWN";
+}
+
+const char *bastion_status_str(bastion_status s) { return bastion_status_string(s); }
+
+bastion_status bastion_read_error(const uint32_t *dev_err, uint32_t *host_word, bastion_stream_t stream) {
+  if (!dev_err || !host_word) return fail(BASTION_ERR_INVALID_ARG, "read_error: NULL pointer");
+  cudaError_t e = cudaMemcpyAsync(host_word, dev_err, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "read_error copy");
+  return BASTION_OK;
+}
+
+bastion_status bastion_error_status(uint32_t word) {
+  if (word == 0u) return BASTION_OK;
+  if (word & BASTION_DEVERR_TIMEOUT) return fail(BASTION_ERR_TIMEOUT, "device error word: an in-kernel wait expired");
+  return fail(BASTION_ERR_DEVICE, "device error word: bad data (bits " + std::to_string(word) + ")");
+}
+
+size_t bastion_topk_softmax_workspace_size(int rows, int V, int k) {
+  (void)rows;
+  (void)V;
+  (void)k;
+  return 0;
 }
 
 const char *bastion_last_error(void) { return g_last.c_str(); }

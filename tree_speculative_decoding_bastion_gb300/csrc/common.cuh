@@ -108,6 +108,18 @@ BST_DEV float load_scalar<BF16Tag>(const void *base, int64_t idx) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
+// Element `idx` of a row staged in shared memory, as float (exact).
+template <class Tag>
+BST_DEV float load_scalar_shared(const uint8_t *stage, int idx);
+template <>
+BST_DEV float load_scalar_shared<F32Tag>(const uint8_t *stage, int idx) {
+  return reinterpret_cast<const float *>(stage)[idx];
+}
+template <>
+BST_DEV float load_scalar_shared<BF16Tag>(const uint8_t *stage, int idx) {
+  return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(stage)[idx]) << 16);
+}
+
 // Streaming 16-byte load that does not allocate in L1 (read-once data).
 BST_DEV uint4 ld_stream16(const void *p) {
   uint4 r;
@@ -119,9 +131,13 @@ BST_DEV uint4 ld_stream16(const void *p) {
 
 // ---------------------------------------------------------------- ordering keys
 // Order-preserving map float -> uint32 (larger float -> larger uint).  Finite
-// floats never map to 0, which therefore marks "empty".
+// floats never map to 0, which therefore marks "empty".  -0.0 and +0.0 compare
+// equal as floats, so they map to the same key (that of +0.0): an ordering by
+// (value, index) then breaks a tie between the two zeros by index, as a
+// comparison of the float values does.
 BST_DEV uint32_t sortable(float f) {
   uint32_t u = __float_as_uint(f);
+  u = (u == 0x80000000u) ? 0u : u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 BST_DEV float unsortable(uint32_t s) {

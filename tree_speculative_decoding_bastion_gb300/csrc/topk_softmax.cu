@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
       pv = packed_v(best);
       pi = packed_i(best);
       if (tid == 0) {
-        sm.new_v[r] = pv;
+        // the element itself (the key maps -0.0 to +0.0)
+        sm.new_v[r] = kBulk ? load_scalar_shared<Tag>(k1_stage, pi - c0) : load_scalar<Tag>(rowp, pi);
         sm.new_i[r] = pi;
       }
       ++got;
@@ -344,6 +345,12 @@ __global__ void __launch_bounds__(K1_THREADS) topk_softmax_kernel(
   }
   cluster.sync();
   if (tid == 0) BST_STAMP(g_k1_trace, 4);
+  if (kBulk && !staged) {
+    // the staged copy timed out: let it land (bounded) before this CTA's
+    // shared memory can go to another CTA
+    int no_abort = 0;
+    mbar_wait(&sm.bar, 0, &no_abort, K1_WAIT_NS);
+  }
   if (crank != 0) return;
 
   // ---- rank 0: the row's lse, then the top k of the C sorted partial lists
