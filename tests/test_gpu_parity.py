@@ -31,6 +31,18 @@ SMALL = {
     "unaligned_bf16": W["qwen3_8b_b1"].scaled(name="unaligned_bf16", B=1, V=5003, K=8, n_min=48, n_max=48, L=200),
     "mha_d64": W["qwen3_8b_b1"].scaled(name="mha_d64", B=2, V=4096, K=6, topk=4, n_min=30, n_max=30, Hq=2, Hkv=2,
                                        d=64, L=300),
+    # CTA pairs over paged caches: 64-key halves made of 8-, 32- or 64-token
+    # pages; 128-token pages take the single-CTA form; three M-tiles (the
+    # second pair half empty)
+    "paged_p8": W["llama31_8b_b16_paged"].scaled(name="paged_p8", B=2, V=4096, L=500, L_min=100, page_size=8,
+                                                 n_min=40, n_max=40),
+    "paged_p32": W["llama31_8b_b16_paged"].scaled(name="paged_p32", B=2, V=4096, L=700, L_min=90, page_size=32,
+                                                  n_min=80, n_max=96),
+    "paged_p64": W["llama31_8b_b16_paged"].scaled(name="paged_p64", B=2, V=4096, L=900, L_min=300, page_size=64,
+                                                  n_min=60, n_max=64),
+    "paged_p128": W["llama31_8b_b16_paged"].scaled(name="paged_p128", B=2, V=4096, L=800, L_min=129, page_size=128,
+                                                   n_min=50, n_max=64),
+    "pair_3tiles": W["qwen3_8b_b1"].scaled(name="pair_3tiles", B=2, V=4096, K=8, L=333, n_min=96, n_max=96),
 }
 FULL = ["tiny_v1024_f32", "qwen3_8b_b1", "llama31_8b_b16_paged", "long_ctx_b4", "controller_sweep_peaked",
         "controller_sweep_flat"]

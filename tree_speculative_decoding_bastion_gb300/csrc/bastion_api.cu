@@ -33,10 +33,12 @@ cudaError_t launch_accept(const void *target, bool bf16, int B, int n_max, int V
                           uint32_t *dev_err, int num_sms, cudaStream_t stream);
 struct AttnPlan {
   int mtiles, splits, tiles_per_split;
+  int pair;   // 1: CTA pairs (cta_group::2): K tensor maps load 64-key boxes
   int64_t cap;
   size_t ws_bytes, off_o, off_ml;
 };
-AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, int num_sms, bool paged);
+AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, int num_sms, bool paged,
+                        int page_size);
 cudaError_t launch_tree_attn_tc(const CUtensorMap *maps, const AttnPlan &pl, int B, int n_max, int Hq, int Hkv, int d,
                                 float scale, bool paged, int page_size, int max_pages, int num_pages,
                                 const int32_t *ctx_len, const int32_t *n, const uint64_t *mask,
@@ -282,7 +284,8 @@ size_t bastion_tree_attn_workspace_size(int B, int n_max, int Hq, int Hkv, int d
   if (!kv || B < 1 || n_max < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (d != 64 && d != 128)) return 0;
   int sms = 0;
   if (current_device(&sms) != BASTION_OK) return 0;
-  return bst::plan_tree_attn(B, n_max, Hq, Hkv, d, kv_capacity(kv), sms, kv->block_table != nullptr).ws_bytes;
+  return bst::plan_tree_attn(B, n_max, Hq, Hkv, d, kv_capacity(kv), sms, kv->block_table != nullptr, kv->page_size)
+      .ws_bytes;
 }
 
 bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *v_tree, bastion_dtype dtype, int B,
@@ -326,7 +329,9 @@ bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *
   if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(kv->k) || !aligned16(kv->v) ||
       !aligned16(out))
     return fail(BASTION_ERR_INVALID_ARG, "tree_attn: bf16 tensors must be 16-byte aligned");
-  const bst::AttnPlan pl = bst::plan_tree_attn(B, n_max, Hq, Hkv, d, cap, sms, paged);
+  const bst::AttnPlan pl = bst::plan_tree_attn(B, n_max, Hq, Hkv, d, cap, sms, paged, kv->page_size);
+  // a CTA pair loads half the keys of every K tile per CTA
+  const cuuint32_t k_rows = pl.pair ? 64 : 128;
   if (pl.ws_bytes > 0 && (!ws || ws_bytes < pl.ws_bytes || !aligned16(ws)))
     return fail(BASTION_ERR_WORKSPACE, "tree_attn: workspace too small (need " + std::to_string(pl.ws_bytes) + " bytes)");
 
@@ -339,12 +344,13 @@ bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(128 / g)};
     if (!encode_bf16(&maps[0], q, 3, dims, strides, box)) return fail(BASTION_ERR_CUDA, "tree_attn: Q tensor map");
   }
-  if (!paged) {  // K/V [B*Hkv][L_max][d]: box 64 x 128 x 1
+  if (!paged) {  // K/V [B*Hkv][L_max][d]: box 64 x 128 x 1 (K of a CTA pair: 64 x 64 x 1)
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kv->L_max),
                                 static_cast<cuuint64_t>(B) * Hkv};
     const cuuint64_t strides[2] = {d * es, static_cast<cuuint64_t>(kv->L_max) * d * es};
+    const cuuint32_t kbox[3] = {64, k_rows, 1};
     const cuuint32_t box[3] = {64, 128, 1};
-    if (!encode_bf16(&maps[1], kv->k, 3, dims, strides, box) || !encode_bf16(&maps[2], kv->v, 3, dims, strides, box))
+    if (!encode_bf16(&maps[1], kv->k, 3, dims, strides, kbox) || !encode_bf16(&maps[2], kv->v, 3, dims, strides, box))
       return fail(BASTION_ERR_CUDA, "tree_attn: KV tensor map");
   } else {  // pages [num_pages][Hkv][page_size][d]: box 64 x page_size x 1 x 1
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kv->page_size),
@@ -355,12 +361,13 @@ bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *
     if (!encode_bf16(&maps[1], kv->k, 4, dims, strides, box) || !encode_bf16(&maps[2], kv->v, 4, dims, strides, box))
       return fail(BASTION_ERR_CUDA, "tree_attn: paged KV tensor map");
   }
-  {  // tree K/V [B*n_max][Hkv][d]: box 64 x 1 x 128
+  {  // tree K/V [B*n_max][Hkv][d]: box 64 x 1 x 128 (K of a CTA pair: 64 x 1 x 64)
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv),
                                 static_cast<cuuint64_t>(B) * n_max};
     const cuuint64_t strides[2] = {d * es, static_cast<cuuint64_t>(Hkv) * d * es};
+    const cuuint32_t kbox[3] = {64, 1, k_rows};
     const cuuint32_t box[3] = {64, 1, 128};
-    if (!encode_bf16(&maps[3], k_tree, 3, dims, strides, box) || !encode_bf16(&maps[4], v_tree, 3, dims, strides, box))
+    if (!encode_bf16(&maps[3], k_tree, 3, dims, strides, kbox) || !encode_bf16(&maps[4], v_tree, 3, dims, strides, box))
       return fail(BASTION_ERR_CUDA, "tree_attn: tree KV tensor map");
   }
   cudaError_t e = bst::launch_tree_attn_tc(maps, pl, B, n_max, Hq, Hkv, d, scale, paged, kv->page_size, kv->max_pages,

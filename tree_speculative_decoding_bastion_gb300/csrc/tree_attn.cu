@@ -10,21 +10,24 @@
 //     out = softmax(q . keys * scale) . values.
 //
 // bf16 path (tcgen05): one CTA per (request b, KV head, 128-row M-tile, KV
-// split).  The M rows pack g = Hq/Hkv query heads x tree nodes of one KV head
-// (GQA), so every K/V tile is used by all heads of its group.  Roles:
-//   warp 4      TMA producer: Q once, then K tiles (128 keys, 3-stage ring,
-//               running one tile ahead) and V tiles (3-stage ring), 128-byte
-//               swizzle; paged caches are gathered page by page through a 4-D
-//               tensor map; no multicast.
-//   warp 5      MMA issuer (one thread): S = Q K^T into TMEM (three S
+// split), or one CTA pair per two M-tiles (see the kernel).  The M rows pack
+// g = Hq/Hkv query heads x tree nodes of one KV head (GQA), so every K/V tile
+// is used by all heads of its group.  Roles:
+//   warp 8      TMA producer: Q once, then K tiles (128 keys, running one
+//               tile ahead) and V tiles, in rings, 128-byte swizzle; paged
+//               caches are gathered page by page through a 4-D tensor map;
+//               no multicast.
+//   warp 9      MMA issuer (one thread): S = Q K^T into TMEM (three S
 //               buffers, each freed by its own barrier once the P V that
 //               read it finished), O += P V with P read from TMEM (P aliases
 //               its S buffer).
-//   warps 0-3   softmax: thread r owns TMEM lane r = M-tile row r; it reads S,
-//               applies the context bound or the ancestor bits, keeps the
-//               running max / sum in the log2 domain, writes P (bf16) to TMEM,
-//               and rescales O only when its row max grew by more than 2^8
-//               (the exact result is the same for any running reference max).
+//   warps 0-7   softmax: warps q and q + 4 own TMEM lanes 32q..32q+31 (M-tile
+//               rows), each one half of the columns; they read S, apply the
+//               context bound or the ancestor bits, swap half-row maxima,
+//               keep the running max / sum in the log2 domain, write P
+//               (bf16) to TMEM, and rescale O only when a row max grew by
+//               more than 2^8 (the exact result is the same for any running
+//               reference max).
 // A request's context tiles followed by its tree tiles are spread evenly over
 // the KV splits.  The splits of one (b, kvh, M-tile) form one thread-block
 // cluster: each CTA stores its partial (O, m, l) to the workspace in L2, one
@@ -48,12 +51,14 @@ namespace cg = cooperative_groups;
 
 namespace bst {
 
-constexpr int ATT_THREADS = 192;
+constexpr int ATT_THREADS = 320;        // 8 softmax warps, a TMA warp, an MMA warp
+constexpr int ATT_TMA_WARP = 8;
+constexpr int ATT_MMA_WARP = 9;
 constexpr int ATT_N = 128;              // keys per tile
 constexpr int ATT_M = 128;              // rows per M-tile
 constexpr int ATT_HALF = ATT_N * 128;   // bytes of 128 rows x 64 bf16
-constexpr int ATT_KSTAGES = 3;
-constexpr int ATT_VSTAGES = 3;
+constexpr int ATT_VSTAGES = 3;         // V ring depth of the single-CTA form (head_dim 64)
+constexpr int ATT_MAX_STAGES = 4;      // of either form
 constexpr int ATT_SBUF = 3;             // S / P buffers in TMEM (128 columns each; O follows)
 constexpr int ATT_MAX_SPLITS = 16;      // cluster size; above 8 (non-portable) where the device keeps them resident
 constexpr uint64_t ATT_WAIT_NS = 200ull * 1000ull * 1000ull;
@@ -75,28 +80,43 @@ struct AttnParams {
 
 struct AttnBars {
   uint64_t q_full;
-  uint64_t k_full[ATT_KSTAGES];
-  uint64_t k_empty[ATT_KSTAGES];
-  uint64_t v_full[ATT_VSTAGES];
-  uint64_t v_empty[ATT_VSTAGES];
-  uint64_t s_full[ATT_SBUF];
+  uint64_t k_full[ATT_MAX_STAGES];
+  uint64_t v_full[ATT_MAX_STAGES];
+  uint64_t v_empty[ATT_MAX_STAGES];   // P V(j) finished (V stage j free, O updated)
+  uint64_t s_full[ATT_SBUF];          // S(j) finished (S ready, K stage j mod 3 free)
   uint64_t p_full[ATT_SBUF];
-  uint64_t s_free[ATT_SBUF];   // the P V that read buffer b finished
-  uint64_t o_done;
   uint64_t drain;
+  // the two softmax warps that share a row quarter (warps q and q + 4, one
+  // half of the columns each) swap their row maxima every tile, and their
+  // row sums at the end, through xmax / xl; xbar[q] completes once per swap
+  uint64_t xbar[4];
+  float xmax[2][2][ATT_M];   // [tile parity][column half][row]
+  float xl[2][ATT_M];        // [column half][row]
   uint32_t tmem_base;
   int abort;
 };
 
-template <int D>
+template <int D, bool kPair>
 struct AttnLayout {
   static constexpr int NH = D / 64;
+  // a CTA pair needs head_dim 128: each CTA holds one 64-column half of V
+  static_assert(!kPair || D == 128, "the CTA-pair form needs head_dim 128");
+  // K stage j mod 3 is S buffer j mod 3 (one barrier serves both)
+  static constexpr int KSTAGES = ATT_SBUF;
+  // (a single CTA with head_dim 128 keeps two V tiles: three do not fit next
+  // to three K tiles, Q and the barriers)
+  static constexpr int VSTAGES = kPair ? 4 : (D == 128 ? 2 : ATT_VSTAGES);
   static constexpr int Q_BYTES = NH * ATT_HALF;
-  static constexpr int KV_BYTES = NH * ATT_HALF;
+  // one CTA's part of a K tile: 128 keys (alone) or its 64 keys (pair), each
+  // as NH column halves of 64 d; of a V tile: every d half (alone) or its one
+  // half (pair), 128 keys each
+  static constexpr int K_HALF = kPair ? ATT_HALF / 2 : ATT_HALF;
+  static constexpr int K_BYTES = NH * K_HALF;
+  static constexpr int V_BYTES = kPair ? ATT_HALF : NH * ATT_HALF;
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_BYTES;
-  static constexpr int V_OFF = K_OFF + ATT_KSTAGES * KV_BYTES;
-  static constexpr int BAR_OFF = V_OFF + ATT_VSTAGES * KV_BYTES;
+  static constexpr int V_OFF = K_OFF + KSTAGES * K_BYTES;
+  static constexpr int BAR_OFF = V_OFF + VSTAGES * V_BYTES;
 
   static constexpr int USED = BAR_OFF + static_cast<int>(sizeof(AttnBars));
   // 1024 bytes of slack for aligning the dynamic shared memory base; at least
@@ -220,12 +240,24 @@ BST_DEV void merge_splits(const AttnParams &p, int b, int kvh, int mtile, int sp
   }
 }
 
-template <int D, bool kPaged>
+// kPair = false: one CTA per (request, KV head, 128-row M-tile, KV split).
+// kPair = true: the two M-tiles 2p and 2p+1 of a (request, KV head) run as a
+// CTA pair (cta_group::2) on two SMs: each CTA loads its own 128 rows of Q,
+// half the keys of every K tile (64 of 128) and one 64-column half of every V
+// tile, and the leader (even) CTA issues M = 256 MMAs that read both CTAs'
+// shared memory and write both CTAs' TMEM.  Every K/V byte then crosses L2 to
+// one SM instead of two, and each SM's shared memory feeds half of the B
+// operand.  The pair's copies complete on the leader's barriers; the leader's
+// commits arrive on both CTAs' barriers; the peer's softmax warps arrive on
+// the leader's P barrier remotely.
+template <int D, bool kPaged, bool kPair>
 __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kt,
     const __grid_constant__ CUtensorMap tm_vt, const AttnParams p) {
-  using LY = AttnLayout<D>;
+  using LY = AttnLayout<D, kPair>;
+  constexpr int KS = LY::KSTAGES;
+  constexpr int VS = LY::VSTAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sQ = smem + LY::Q_OFF;
@@ -234,13 +266,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   cg::cluster_group cluster = cg::this_cluster();
 
   const int mtile = blockIdx.x;
-  const int split = blockIdx.y;   // the cluster spans the splits (blockIdx.y)
+  const int split = blockIdx.y;   // the cluster spans the splits (blockIdx.y), and the pair (blockIdx.x)
   const int bh = blockIdx.z;
   const int b = bh / p.Hkv;
   const int kvh = bh - b * p.Hkv;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
+  // CTA pair: the peer CTA's %cluster_ctarank differs in bit 0 (blockIdx.x & 1)
+  const uint32_t crank = kPair ? cluster_ctarank() : 0u;
+  const uint32_t lead_rank = crank & ~1u;
+  const int half = kPair ? (blockIdx.x & 1) : 0;   // which half of each K and V tile this CTA loads
+  const bool leader = half == 0;
+  const uint16_t pair_mask = static_cast<uint16_t>(3u << lead_rank);
 
   if (tid == 0) BST_TRACE_AT(0);
   // private set-up first (barriers, descriptor prefetch), then the wait for
@@ -248,18 +286,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   if (tid == 0) {
     mbar_init(&bars->q_full, 1);
 #pragma unroll
-    for (int i = 0; i < ATT_KSTAGES; ++i) mbar_init(&bars->k_full[i], 1), mbar_init(&bars->k_empty[i], 1);
+    for (int i = 0; i < KS; ++i) mbar_init(&bars->k_full[i], 1);
 #pragma unroll
-    for (int i = 0; i < ATT_VSTAGES; ++i) mbar_init(&bars->v_full[i], 1), mbar_init(&bars->v_empty[i], 1);
+    for (int i = 0; i < VS; ++i) mbar_init(&bars->v_full[i], 1), mbar_init(&bars->v_empty[i], 1);
 #pragma unroll
-    for (int i = 0; i < ATT_SBUF; ++i)
-      mbar_init(&bars->s_full[i], 1), mbar_init(&bars->p_full[i], 128), mbar_init(&bars->s_free[i], 1);
-    mbar_init(&bars->o_done, 1);
+    for (int i = 0; i < ATT_SBUF; ++i)   // P: every softmax thread (alone) or one lane per softmax warp of both CTAs
+      mbar_init(&bars->s_full[i], 1), mbar_init(&bars->p_full[i], kPair ? 16 : 256);
     mbar_init(&bars->drain, 1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->xbar[i], 64);
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == ATT_TMA_WARP && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -280,7 +319,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
     if (tid == 0 && mtile == 0 && split == 0 && kvh == 0) set_err(p.dev_err, BASTION_DEVERR_CTX);
     L = L < 0 ? 0 : static_cast<int>(p.cap);
   }
-  if (mtile * ATT_M >= nb * p.g) return;   // no active row in this M-tile
+  // no active row in this M-tile (alone) or in the pair's first M-tile (pair:
+  // both CTAs take the same exit)
+  if ((kPair ? (mtile & ~1) : mtile) * ATT_M >= nb * p.g) return;
 
   // the request's context tiles followed by its tree tiles, spread evenly
   // over the splits: this split takes tiles [g0, g1)
@@ -294,20 +335,28 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   const int n_tree = max(0, g1 - max(g0, ctx_tiles));
   const int T = n_ctx + n_tree;
 
-  // row owned by a softmax thread
-  const int r = tid;   // valid for tid < 128
+  // row owned by a softmax thread (warps 0-7: row tid mod 128, column half
+  // tid / 128)
+  const int r = tid & (ATT_M - 1);
   const int pidx = mtile * ATT_M + r;
   const int node = pidx / p.g;
-  const bool active = (tid < 128) && (node < nb);
+  const bool active = (tid < 2 * ATT_M) && (node < nb);
 
   float m_run = -CUDART_INF_F;
   float l_run = 0.f;
   bool ok = true;
   uint32_t tbase = 0;
 
+  // a pair's barriers are initialised before either CTA signals the other's
+  if (kPair) cluster_sync_all();
   if (T > 0 && warp == 0) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(&bars->tmem_base, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&bars->tmem_base, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -318,14 +367,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
     tbase = bars->tmem_base;
     const uint32_t tO = tbase + ATT_SBUF * 128;
 
-    if (warp == 4) {
+    if (warp == ATT_TMA_WARP) {
       // ------------------------------------------------ TMA producer
       if (lane == 0) {
         BST_TRACE_AT(2);
-        mbar_expect_tx(&bars->q_full, LY::Q_BYTES);
+        // a copy completes on this CTA's barrier (alone) or on the leader's
+        // (pair: the leader expects both CTAs' bytes)
+        auto tma3 = [&](void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1, int c2) {
+          if (kPair)
+            tma_load_3d_pair(dst, m, mapa_shared(bar, lead_rank), c0, c1, c2);
+          else
+            tma_load_3d(dst, m, bar, c0, c1, c2);
+        };
+        auto tma4 = [&](void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1, int c2, int c3) {
+          if (kPair)
+            tma_load_4d_pair(dst, m, mapa_shared(bar, lead_rank), c0, c1, c2, c3);
+          else
+            tma_load_4d(dst, m, bar, c0, c1, c2, c3);
+        };
+        constexpr uint32_t TX_MUL = kPair ? 2u : 1u;
+        if (leader) mbar_expect_tx(&bars->q_full, TX_MUL * LY::Q_BYTES);
 #pragma unroll
         for (int h = 0; h < LY::NH; ++h)
-          tma_load_3d(sQ + h * ATT_HALF, &tm_q, &bars->q_full, h * 64, kvh * p.g, b * p.n_max + mtile * (ATT_M / p.g));
+          tma3(sQ + h * ATT_HALF, &tm_q, &bars->q_full, h * 64, kvh * p.g, b * p.n_max + mtile * (ATT_M / p.g));
         // Paged caches: the page ids of a context tile are read from the block
         // table with all loads in flight together, one K tile ahead of the copy
         // that needs them, so their latency hides behind the previous tile; the
@@ -345,44 +409,79 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
                           : PG_BEYOND;
           }
         };
-        // one K or V tile (context or tree) into `dst`, completing on `fb`;
-        // pg: the tile's page ids (paged context tiles)
-        auto load_tile = [&](int j, bool is_v, uint8_t *dst, uint64_t *fb, const int (&pg)[MAXPG]) {
-          const CUtensorMap *mc = is_v ? &tm_v : &tm_k;
-          const CUtensorMap *mt = is_v ? &tm_vt : &tm_kt;
+        // checked page id (out of range: the copy reads zeros and the error
+        // word says so)
+        auto page_of = [&](int page) {
+          if (page == PG_BEYOND) return p.num_pages;
+          if (page < 0 || page >= p.num_pages) {
+            set_err(p.dev_err, BASTION_DEVERR_PAGE);
+            return p.num_pages;
+          }
+          return page;
+        };
+        // This CTA's part of K tile j (context or tree) into `dst`, completing
+        // on `fb`: all 128 keys (alone) or keys [64 half, 64 half + 64) (pair),
+        // as LY::NH column halves of 64 d.  pg: the tile's page ids.
+        auto load_k = [&](int j, uint8_t *dst, uint64_t *fb, const int (&pg)[MAXPG]) {
+          const int key0 = kPair ? half * (ATT_N / 2) : 0;
           if (j < n_ctx) {
             const int ct = ct0 + j;
             if (!kPaged) {
 #pragma unroll
-              for (int h = 0; h < LY::NH; ++h) tma_load_3d(dst + h * ATT_HALF, mc, fb, h * 64, ct * ATT_N, b * p.Hkv + kvh);
+              for (int h = 0; h < LY::NH; ++h)
+                tma3(dst + h * LY::K_HALF, &tm_k, fb, h * 64, ct * ATT_N + key0, b * p.Hkv + kvh);
             } else {
               const int ps = p.page_size;
+              const int np = (kPair ? ATT_N / 2 : ATT_N) / ps;   // pages of this CTA's keys
+              const int pi0 = key0 / ps;
 #pragma unroll
-              for (int pi = 0; pi < MAXPG; ++pi) {
-                if (pi * ps >= ATT_N) break;
-                int page = pg[pi];
-                if (page == PG_BEYOND) {
-                  page = p.num_pages;   // out of range: the copy reads zeros
-                } else if (page < 0 || page >= p.num_pages) {
-                  set_err(p.dev_err, BASTION_DEVERR_PAGE);
-                  page = p.num_pages;
-                }
+              for (int pj = 0; pj < MAXPG; ++pj) {
+                if (pj >= np) break;
+                const int page = page_of(pg[pi0 + pj]);
 #pragma unroll
-                for (int h = 0; h < LY::NH; ++h) tma_load_4d(dst + h * ATT_HALF + pi * ps * 128, mc, fb, h * 64, 0, kvh, page);
+                for (int h = 0; h < LY::NH; ++h) tma4(dst + h * LY::K_HALF + pj * ps * 128, &tm_k, fb, h * 64, 0, kvh, page);
               }
             }
           } else {
             const int tt = tr0 + j - n_ctx;
 #pragma unroll
-            for (int h = 0; h < LY::NH; ++h) tma_load_3d(dst + h * ATT_HALF, mt, fb, h * 64, kvh, b * p.n_max + tt * ATT_N);
+            for (int h = 0; h < LY::NH; ++h)
+              tma3(dst + h * LY::K_HALF, &tm_kt, fb, h * 64, kvh, b * p.n_max + tt * ATT_N + key0);
+          }
+        };
+        // This CTA's part of V tile j: every d half (alone) or d half `half`
+        // (pair), all 128 keys.
+        auto load_v = [&](int j, uint8_t *dst, uint64_t *fb, const int (&pg)[MAXPG]) {
+          constexpr int NVH = kPair ? 1 : LY::NH;
+          if (j < n_ctx) {
+            const int ct = ct0 + j;
+            if (!kPaged) {
+#pragma unroll
+              for (int h = 0; h < NVH; ++h)
+                tma3(dst + h * ATT_HALF, &tm_v, fb, (h + half) * 64, ct * ATT_N, b * p.Hkv + kvh);
+            } else {
+              const int ps = p.page_size;
+#pragma unroll
+              for (int pi = 0; pi < MAXPG; ++pi) {
+                if (pi * ps >= ATT_N) break;
+                const int page = page_of(pg[pi]);
+#pragma unroll
+                for (int h = 0; h < NVH; ++h) tma4(dst + h * ATT_HALF + pi * ps * 128, &tm_v, fb, (h + half) * 64, 0, kvh, page);
+              }
+            }
+          } else {
+            const int tt = tr0 + j - n_ctx;
+#pragma unroll
+            for (int h = 0; h < NVH; ++h)
+              tma3(dst + h * ATT_HALF, &tm_vt, fb, (h + half) * 64, kvh, b * p.n_max + tt * ATT_N);
           }
         };
         int k_issued = 0, v_issued = 0;
         auto issue_k = [&](int j) -> bool {
-          const int st = j % ATT_KSTAGES;
-          if (j >= ATT_KSTAGES && !mbar_wait(&bars->k_empty[st], ((j / ATT_KSTAGES) - 1) & 1, abort, ATT_WAIT_NS))
-            return false;
-          mbar_expect_tx(&bars->k_full[st], LY::KV_BYTES);
+          const int st = j % KS;
+          // the stage is free once S(j - KS), which read it, is complete
+          if (j >= KS && !mbar_wait(&bars->s_full[st], ((j / KS) - 1) & 1, abort, ATT_WAIT_NS)) return false;
+          if (leader) mbar_expect_tx(&bars->k_full[st], TX_MUL * LY::K_BYTES);
           if (kPaged) {
 #pragma unroll
             for (int pi = 0; pi < MAXPG; ++pi) {
@@ -391,18 +490,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
             }
             fetch_pages(j + 1);
           }
-          load_tile(j, false, smem + LY::K_OFF + st * LY::KV_BYTES, &bars->k_full[st], pgB);
+          load_k(j, smem + LY::K_OFF + st * LY::K_BYTES, &bars->k_full[st], pgB);
           if (j < 8) BST_TRACE_AT(32 + j);
           k_issued = j + 1;
           return true;
         };
         auto issue_v = [&](int j) -> bool {
-          const int st = j % ATT_VSTAGES;
-          if (j >= ATT_VSTAGES && !mbar_wait(&bars->v_empty[st], ((j / ATT_VSTAGES) - 1) & 1, abort, ATT_WAIT_NS))
-            return false;
-          mbar_expect_tx(&bars->v_full[st], LY::KV_BYTES);
+          const int st = j % VS;
+          if (j >= VS && !mbar_wait(&bars->v_empty[st], ((j / VS) - 1) & 1, abort, ATT_WAIT_NS)) return false;
+          if (leader) mbar_expect_tx(&bars->v_full[st], TX_MUL * LY::V_BYTES);
           // V(j) follows K(j + 1) unless j is the last tile
-          load_tile(j, true, smem + LY::V_OFF + st * LY::KV_BYTES, &bars->v_full[st], j + 1 < T ? pgA : pgB);
+          load_v(j, smem + LY::V_OFF + st * LY::V_BYTES, &bars->v_full[st], j + 1 < T ? pgA : pgB);
           if (j < 8) BST_TRACE_AT(48 + j);
           v_issued = j + 1;
           return true;
@@ -416,78 +514,118 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         }
         if (*abort) {
           // let the copies already in flight land before the CTA goes away
-          for (int j = max(0, k_issued - ATT_KSTAGES); j < k_issued; ++j)
-            mbar_wait(&bars->k_full[j % ATT_KSTAGES], (j / ATT_KSTAGES) & 1, abort, ATT_WAIT_NS);
-          for (int j = max(0, v_issued - ATT_VSTAGES); j < v_issued; ++j)
-            mbar_wait(&bars->v_full[j % ATT_VSTAGES], (j / ATT_VSTAGES) & 1, abort, ATT_WAIT_NS);
-          mbar_wait(&bars->q_full, 0, abort, ATT_WAIT_NS);
+          // (a pair's copies complete on the leader's barriers: the leader
+          // waits for both CTAs' bytes; the peer stays until the final
+          // cluster barrier)
+          if (leader) {
+            for (int j = max(0, k_issued - KS); j < k_issued; ++j)
+              mbar_wait(&bars->k_full[j % KS], (j / KS) & 1, abort, ATT_WAIT_NS);
+            for (int j = max(0, v_issued - VS); j < v_issued; ++j)
+              mbar_wait(&bars->v_full[j % VS], (j / VS) & 1, abort, ATT_WAIT_NS);
+            mbar_wait(&bars->q_full, 0, abort, ATT_WAIT_NS);
+          }
         }
       }
-    } else if (warp == 5) {
-      // ------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t IDESC_QK = idesc_bf16(ATT_M, ATT_N, 0);
-        constexpr uint32_t IDESC_PV = idesc_bf16(ATT_M, D, 1);
+    } else if (warp == ATT_MMA_WARP) {
+      // ------------------------------------------------ MMA issuer (the leader of a pair)
+      if (lane == 0 && leader) {
+        constexpr int MM = kPair ? 2 * ATT_M : ATT_M;
+        constexpr uint32_t IDESC_QK = idesc_bf16(MM, ATT_N, 0);
+        constexpr uint32_t IDESC_PV = idesc_bf16(MM, D, 1);
         const uint32_t q_addr = smem_u32(sQ);
+        auto commit = [&](uint64_t *bar) {
+          if (kPair)
+            mma_commit_pair(bar, pair_mask);
+          else
+            mma_commit(bar);
+        };
+        auto mma_ss_ = [&](uint32_t d_, uint64_t a_, uint64_t b_, uint32_t i_, uint32_t acc) {
+          if (kPair)
+            mma_ss_pair(d_, a_, b_, i_, acc);
+          else
+            mma_ss(d_, a_, b_, i_, acc);
+        };
+        auto mma_ts_ = [&](uint32_t d_, uint32_t a_, uint64_t b_, uint32_t i_, uint32_t acc) {
+          if (kPair)
+            mma_ts_pair(d_, a_, b_, i_, acc);
+          else
+            mma_ts(d_, a_, b_, i_, acc);
+        };
         bool any = false;
+        // S(jj) = Q K(jj)^T into S buffer jj mod 3, which is also K stage
+        // jj mod 3: one commit tells the softmax that S is ready and the
+        // producer that the K stage is free
+        auto issue_qk = [&](int jj) -> bool {
+          const int ks = jj % KS;
+          if (!mbar_wait(&bars->k_full[ks], (jj / KS) & 1, abort, ATT_WAIT_NS)) return false;
+          if (jj < 8) BST_TRACE_AT(40 + jj);
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + LY::K_OFF + ks * LY::K_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int h = kk >> 2;
+            const uint64_t adesc = sdesc_sw128(q_addr + h * ATT_HALF + (kk & 3) * 32, 16, 1024);
+            const uint64_t bdesc = sdesc_sw128(k_addr + h * LY::K_HALF + (kk & 3) * 32, 16, 1024);
+            mma_ss_(tbase + ks * 128, adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          any = true;
+          commit(&bars->s_full[ks]);
+          BST_TRACE_AT(3 + min(jj, 7));
+          return true;
+        };
+        // O += P(jj) V(jj); one commit frees the V stage and tells the softmax
+        // that O holds P(jj) V(jj) (before it rescales O)
         auto issue_pv = [&](int jj) -> bool {
           const int sb = jj % ATT_SBUF;
-          const int vs = jj % ATT_VSTAGES;
+          const int vs = jj % VS;
+          // P arrives from this CTA's softmax threads (alone) or from one lane
+          // of each softmax warp of both CTAs (pair)
           if (!mbar_wait(&bars->p_full[sb], (jj / ATT_SBUF) & 1, abort, ATT_WAIT_NS)) return false;
-          if (!mbar_wait(&bars->v_full[vs], (jj / ATT_VSTAGES) & 1, abort, ATT_WAIT_NS)) return false;
+          if (!mbar_wait(&bars->v_full[vs], (jj / VS) & 1, abort, ATT_WAIT_NS)) return false;
           if (jj < 8) BST_TRACE_AT(56 + jj);
           tc_fence_after();
-          const uint32_t v_addr = smem_u32(smem + LY::V_OFF + vs * LY::KV_BYTES);
+          const uint32_t v_addr = smem_u32(smem + LY::V_OFF + vs * LY::V_BYTES);
 #pragma unroll
           for (int kk = 0; kk < ATT_N / 16; ++kk) {
-            // V is the MN-major B operand: 8 keys per 1024-byte swizzle group,
-            // the two 64-column halves of d are ATT_HALF bytes apart.
+            // V is the MN-major B operand: 8 keys per 1024-byte swizzle group;
+            // alone, the two 64-column halves of d are ATT_HALF bytes apart;
+            // in a pair each CTA holds its one half (N split across the pair)
             const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, ATT_HALF, 1024);
-            mma_ts(tO, tbase + sb * 128 + kk * 8, bdesc, IDESC_PV, (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_(tO, tbase + sb * 128 + kk * 8, bdesc, IDESC_PV, (jj > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&bars->o_done);
-          mma_commit(&bars->s_free[sb]);
-          mma_commit(&bars->v_empty[vs]);
+          commit(&bars->v_empty[vs]);
           return true;
         };
         bool run = mbar_wait(&bars->q_full, 0, abort, ATT_WAIT_NS);
         tc_fence_after();
+        // S runs three tiles ahead of P V, so the tensor pipe has work queued
+        // while the softmax turns S(j) into P(j).  S(j + 3) reuses the buffer
+        // of S(j) / P(j); it is issued after P V(j), which read P(j) there, and
+        // the tcgen05.mma of one thread execute in issue order.
+        for (int j = 0; run && j < min(T, ATT_SBUF); ++j) run = issue_qk(j);
         for (int j = 0; run && j < T; ++j) {
-          const int ks = j % ATT_KSTAGES;
-          const int sb = j % ATT_SBUF;
-          if (!mbar_wait(&bars->k_full[ks], (j / ATT_KSTAGES) & 1, abort, ATT_WAIT_NS)) { run = false; break; }
-          if (j < 8) BST_TRACE_AT(40 + j);
-          // S buffer sb is free once P_{j-3} V_{j-3} (which read P from it) finished
-          if (j >= ATT_SBUF && !mbar_wait(&bars->s_free[sb], ((j / ATT_SBUF) - 1) & 1, abort, ATT_WAIT_NS)) {
-            run = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + LY::K_OFF + ks * LY::KV_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int h = kk >> 2;
-            const uint32_t off = h * ATT_HALF + (kk & 3) * 32;
-            const uint64_t adesc = sdesc_sw128(q_addr + off, 16, 1024);
-            const uint64_t bdesc = sdesc_sw128(k_addr + off, 16, 1024);
-            mma_ss(tbase + sb * 128, adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
-          }
-          any = true;
-          mma_commit(&bars->s_full[sb]);
-          mma_commit(&bars->k_empty[ks]);
-          BST_TRACE_AT(3 + min(j, 7));
-          if (j >= 1 && !issue_pv(j - 1)) { run = false; break; }
+          if (!issue_pv(j)) { run = false; break; }
+          if (j + ATT_SBUF < T && !issue_qk(j + ATT_SBUF)) { run = false; break; }
         }
-        if (run) issue_pv(T - 1);
         if (any) {
           // every MMA issued above has finished before TMEM is released
-          mma_commit(&bars->drain);
+          commit(&bars->drain);
           mbar_wait(&bars->drain, 0, abort, ATT_WAIT_NS);
         }
       }
     } else {
-      // ------------------------------------------------ softmax warps 0-3
-      const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+      // ------------------------------------------------ softmax warps 0-7
+      // Warp w owns TMEM lanes 32 (w mod 4) .. +31 (rows) and column half
+      // ch = w / 4: keys [64 ch, 64 ch + 64) of every S tile, P columns
+      // [32 ch, 32 ch + 32), O columns [D/2 ch, D/2 ch + D/2).  Two warps per
+      // scheduler hide each other's TMEM and MUFU latency.  Per tile they
+      // swap half-row maxima (so both take the same reference max and
+      // rescale decision) and at the end their half-row sums.
+      constexpr int HC = ATT_N / 2;    // S columns per warp
+      constexpr int DH = D / 2;        // O columns per warp
+      const int rq = warp & 3;
+      const int ch = warp >> 2;
+      const uint32_t lane_off = static_cast<uint32_t>(rq * 32) << 16;
       const int W = (p.n_max + 63) >> 6;
       unsigned long long mw[4] = {0ull, 0ull, 0ull, 0ull};
       if (active) {
@@ -495,46 +633,49 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         for (int w = 0; w < W; ++w) mw[w] = mrow[w];
       }
       const float cs = p.scale_log2;
+      uint64_t *xb = &bars->xbar[rq];
       for (int j = 0; j < T; ++j) {
         const int sb = j % ATT_SBUF;
         if (!warp_wait(&bars->s_full[sb], (j / ATT_SBUF) & 1, abort)) { ok = false; break; }
         tc_fence_after();
         if (tid == 0) BST_TRACE_AT(11 + min(j, 7));
-        uint32_t s[ATT_N];
-        tmem_ld32(tbase + lane_off + sb * 128 + 0, s + 0);
-        tmem_ld32(tbase + lane_off + sb * 128 + 32, s + 32);
-        tmem_ld32(tbase + lane_off + sb * 128 + 64, s + 64);
-        tmem_ld32(tbase + lane_off + sb * 128 + 96, s + 96);
+        const uint32_t scol = tbase + lane_off + sb * 128 + ch * HC;
+        uint32_t s[HC];
+        tmem_ld32(scol + 0, s + 0);
+        tmem_ld32(scol + 32, s + 32);
         tmem_wait_ld32(s + 0);
         tmem_wait_ld32(s + 32);
-        tmem_wait_ld32(s + 64);
-        tmem_wait_ld32(s + 96);
         // masking on the raw scores: context tiles are bounded by L, tree
         // tiles by the ancestor bits (masked scores become -inf)
         const uint32_t NEG = 0xff800000u;
         if (j < n_ctx) {
-          const int nvalid = L - (ct0 + j) * ATT_N;
-          if (nvalid < ATT_N) {
+          const int nvalid = L - (ct0 + j) * ATT_N - ch * HC;
+          if (nvalid < HC) {
 #pragma unroll
-            for (int c = 0; c < ATT_N; ++c) s[c] = (c < nvalid) ? s[c] : NEG;
+            for (int c = 0; c < HC; ++c) s[c] = (c < nvalid) ? s[c] : NEG;
           }
         } else {
           const int tt = tr0 + j - n_ctx;
-          const unsigned long long w0 = (tt == 0) ? mw[0] : mw[2];
-          const unsigned long long w1 = (tt == 0) ? mw[1] : mw[3];
+          const unsigned long long wb = mw[2 * tt + ch];
 #pragma unroll
-          for (int c = 0; c < ATT_N; ++c) {
-            const unsigned long long w = (c < 64) ? w0 : w1;
-            s[c] = ((w >> (c & 63)) & 1ull) ? s[c] : NEG;
-          }
+          for (int c = 0; c < HC; ++c) s[c] = ((wb >> c) & 1ull) ? s[c] : NEG;
         }
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(s[i]);
 #pragma unroll
-        for (int c = 8; c < ATT_N; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(s[c]));
-        const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cs;
+        for (int c = 8; c < HC; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(s[c]));
+        const float hmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        // swap half maxima with the partner warp; the arrival also tells it
+        // this warp's TMEM loads of S are complete (its P stores may then
+        // overwrite those columns)
+        bars->xmax[j & 1][ch][r] = hmax;
+        tc_fence_before();
+        mbar_arrive(xb);
+        if (!warp_wait(xb, j & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        const float tmax = fmaxf(hmax, bars->xmax[j & 1][ch ^ 1][r]) * cs;
         const float m_new = fmaxf(m_run, tmax);
         // keep the running reference unless the max grew by more than 2^8
         const bool jump = m_new > m_run + ATT_RESCALE_LOG2;
@@ -544,64 +685,75 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
         float sum[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) sum[i] = 0.f;
-        uint32_t pk[ATT_N / 2];
+        uint32_t pk[HC / 2];
 #pragma unroll
-        for (int c = 0; c < ATT_N; c += 2) {
+        for (int c = 0; c < HC; c += 2) {
           const float p0 = ex2(fmaf(__uint_as_float(s[c]), cs, -msub));
           const float p1 = ex2(fmaf(__uint_as_float(s[c + 1]), cs, -msub));
           sum[(c >> 1) & 7] += p0 + p1;
           pk[c >> 1] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(tbase + lane_off + sb * 128 + 0, pk + 0);
-        tmem_st32(tbase + lane_off + sb * 128 + 32, pk + 32);
+        tmem_st32(tbase + lane_off + sb * 128 + ch * (HC / 2), pk);
         l_run = l_run * alpha + (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
         const bool need = (j >= 1) && jump && (m_run > -CUDART_INF_F);
         if (__any_sync(FULL, need)) {
-          // O must hold P_{j-1} V_{j-1} before it is rescaled
-          if (!warp_wait(&bars->o_done, (j - 1) & 1, abort)) { ok = false; break; }
+          // O must hold P_{j-1} V_{j-1} before it is rescaled (the commit after
+          // that P V arrives on its V stage's barrier)
+          if (!warp_wait(&bars->v_empty[(j - 1) % VS], ((j - 1) / VS) & 1, abort)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < DH / 32; ++cc) {
             uint32_t o[32];
-            tmem_ld32(tO + lane_off + cc * 32, o);
+            tmem_ld32(tO + lane_off + ch * DH + cc * 32, o);
             tmem_wait_ld32(o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tO + lane_off + cc * 32, o);
+            tmem_st32(tO + lane_off + ch * DH + cc * 32, o);
           }
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[sb]);
+        if (kPair) {
+          // one arrival per warp on the leader's barrier, after every lane's
+          // TMEM stores completed
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(&bars->p_full[sb], lead_rank));
+        } else {
+          mbar_arrive(&bars->p_full[sb]);
+        }
         if (tid == 0) BST_TRACE_AT(19 + min(j, 7));
         m_run = m_use;
       }
       // ---- epilogue: O after the last P V (the drain barrier completes once,
-      // after every MMA of this CTA)
+      // after every MMA of this CTA or pair); the two halves' row sums add
       if (ok && !warp_wait(&bars->drain, 0, abort)) ok = false;
       if (tid == 0) BST_TRACE_AT(27);
-      float o[D];
+      bars->xl[ch][r] = l_run;
+      mbar_arrive(xb);
+      if (ok && !warp_wait(xb, T & 1, abort)) ok = false;
+      const float l_row = l_run + bars->xl[ch ^ 1][r];
+      float o[DH];
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < DH / 32; ++cc) {
           uint32_t t32[32];
-          tmem_ld32(tO + lane_off + cc * 32, t32);
+          tmem_ld32(tO + lane_off + ch * DH + cc * 32, t32);
           tmem_wait_ld32(t32);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[cc * 32 + e] = __uint_as_float(t32[e]);
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < D; ++e) o[e] = 0.f;
+        for (int e = 0; e < DH; ++e) o[e] = 0.f;
       }
       if (p.splits == 1) {
         if (ok && active) {
-          const float inv = 1.f / l_run;
+          const float inv = 1.f / l_row;
           const int hl = pidx - node * p.g;
-          uint16_t *dst = p.out + ((static_cast<int64_t>(b) * p.n_max + node) * p.Hq + kvh * p.g + hl) * D;
+          uint16_t *dst = p.out + ((static_cast<int64_t>(b) * p.n_max + node) * p.Hq + kvh * p.g + hl) * D + ch * DH;
 #pragma unroll
-          for (int c = 0; c < D; c += 8) {
+          for (int c = 0; c < DH; c += 8) {
             uint4 v;
             v.x = pack_bf16x2(o[c + 0] * inv, o[c + 1] * inv);
             v.y = pack_bf16x2(o[c + 2] * inv, o[c + 3] * inv);
@@ -611,11 +763,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
           }
         }
       } else {
-        // this split's partial for the merge
+        // this split's partial for the merge (the row's (m, l) by half 0)
         float4 *dp = part_slot<D>(p, b, kvh, mtile, split);
 #pragma unroll
-        for (int c = 0; c < D; c += 4) dp[(c >> 2) * ATT_M + r] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-        dp[(D / 4) * ATT_M + r] = make_float4(ok ? m_run : -CUDART_INF_F, ok ? l_run : 0.f, 0.f, 0.f);
+        for (int c = 0; c < DH; c += 4)
+          dp[((ch * DH + c) >> 2) * ATT_M + r] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        if (ch == 0) dp[(D / 4) * ATT_M + r] = make_float4(ok ? m_run : -CUDART_INF_F, ok ? l_row : 0.f, 0.f, 0.f);
       }
       if (tid == 0) BST_TRACE_AT(28);
     }
@@ -631,13 +784,27 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_tc_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (T > 0 && warp == 0) tmem_dealloc(tbase, 512);
+  if (kPair && *abort && !leader && tid == 0) {
+    // the pair's copies into this CTA complete on the leader's barriers, which
+    // this CTA cannot watch: give any still in flight a bounded time to land
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 2ull * 1000ull * 1000ull) {
+    }
+  }
+  if (T > 0 && warp == 0) {
+    if (kPair)
+      tmem_dealloc_pair(tbase, 512);
+    else
+      tmem_dealloc(tbase, 512);
+  }
   if (T > 0 && *abort && tid == 0) set_err(p.dev_err, BASTION_DEVERR_TIMEOUT);
 
   // ---- merge of the KV splits: the cluster barrier (release / acquire)
-  // publishes every split's partial, then each CTA merges its rows from L2
+  // publishes every split's partial, then each CTA merges its rows from L2.
+  // A pair always meets here too: neither CTA leaves while the other may
+  // still signal it.
+  if (kPair || p.splits > 1) cluster.sync();
   if (p.splits > 1) {
-    cluster.sync();
     if (tid == 0) BST_TRACE_AT(29);
     switch (p.splits) {
       case 2: merge_splits<D, 2>(p, b, kvh, mtile, split, nb); break;
@@ -825,36 +992,53 @@ __global__ void __launch_bounds__(128) tree_attn_f32_kernel(const float *__restr
 // ------------------------------------------------------------------ host side
 struct AttnPlan {
   int mtiles, splits, tiles_per_split;
+  int pair;   // 1: CTA pairs (cta_group::2) over M-tiles 2p, 2p+1
   int64_t cap;
   size_t ws_bytes, off_o, off_ml;
 };
 
-// Clusters of `splits` CTAs of the bf16 kernel that the current device keeps
-// resident at once (cached per device, head_dim, layout and cluster size).
-static int max_active_clusters(int d, bool paged, int splits) {
+template <bool kPair>
+static const void *attn_kernel_fn(int d, bool paged) {
+  if (kPair) {
+    return paged ? reinterpret_cast<const void *>(tree_attn_tc_kernel<128, true, true>)
+                 : reinterpret_cast<const void *>(tree_attn_tc_kernel<128, false, true>);
+  }
+  return d == 128 ? (paged ? reinterpret_cast<const void *>(tree_attn_tc_kernel<128, true, false>)
+                           : reinterpret_cast<const void *>(tree_attn_tc_kernel<128, false, false>))
+                  : (paged ? reinterpret_cast<const void *>(tree_attn_tc_kernel<64, true, false>)
+                           : reinterpret_cast<const void *>(tree_attn_tc_kernel<64, false, false>));
+}
+
+static int attn_smem_bytes(int d, bool pair) {
+  if (pair) return AttnLayout<128, true>::SMEM;
+  return d == 128 ? AttnLayout<128, false>::SMEM : AttnLayout<64, false>::SMEM;
+}
+
+// Clusters of (pair ? 2 : 1) x `splits` CTAs of the bf16 kernel that the
+// current device keeps resident at once (cached per device, head_dim, layout,
+// form and cluster size).
+static int max_active_clusters(int d, bool paged, bool pair, int splits) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int, int>, int> cache;
+  static std::map<std::tuple<int, int, int, int, int>, int> cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  const auto key = std::make_tuple(dev, d, paged ? 1 : 0, splits);
+  const auto key = std::make_tuple(dev, d, paged ? 1 : 0, pair ? 1 : 0, splits);
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
+  const int cx = pair ? 2 : 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1, splits, 1);
+  cfg.gridDim = dim3(cx, splits, 1);
   cfg.blockDim = dim3(ATT_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = d == 128 ? AttnLayout<128>::SMEM : AttnLayout<64>::SMEM;
+  cfg.dynamicSmemBytes = attn_smem_bytes(d, pair);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.x = cx;
   attr[0].val.clusterDim.y = splits;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const void *fn = d == 128 ? (paged ? reinterpret_cast<const void *>(tree_attn_tc_kernel<128, true>)
-                                     : reinterpret_cast<const void *>(tree_attn_tc_kernel<128, false>))
-                            : (paged ? reinterpret_cast<const void *>(tree_attn_tc_kernel<64, true>)
-                                     : reinterpret_cast<const void *>(tree_attn_tc_kernel<64, false>));
+  const void *fn = pair ? attn_kernel_fn<true>(d, paged) : attn_kernel_fn<false>(d, paged);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
@@ -864,24 +1048,34 @@ static int max_active_clusters(int d, bool paged, int splits) {
   return n;
 }
 
-AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, int num_sms, bool paged) {
+AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, int num_sms, bool paged,
+                        int page_size) {
   AttnPlan pl{};
   const int g = Hq / Hkv;
-  pl.mtiles = (n_max * g + ATT_M - 1) / ATT_M;
+  const int mt = (n_max * g + ATT_M - 1) / ATT_M;
+  // Two or more M-tiles per (request, KV head) run as CTA pairs, which halve
+  // the K/V bytes each SM receives per MMA (head_dim 128; paged caches with
+  // pages of at most 64 tokens, so each CTA's 64 keys are whole pages).
+  pl.pair = (d == 128 && mt >= 2 && (!paged || (page_size <= 64 && 64 % page_size == 0))) ? 1 : 0;
+  if (pl.pair && max_active_clusters(d, paged, true, 1) < 1) pl.pair = 0;
+  pl.mtiles = pl.pair ? 2 * ((mt + 1) / 2) : mt;
   pl.cap = cap;
+  const int cx = pl.pair ? 2 : 1;
+  const int max_splits = ATT_MAX_SPLITS / cx;
   const int64_t ctx_tiles = (cap + ATT_N - 1) / ATT_N;
   const int64_t tree_tiles = (n_max + ATT_N - 1) / ATT_N;
-  const int64_t units = static_cast<int64_t>(B) * Hkv * pl.mtiles;
+  const int64_t units = static_cast<int64_t>(B) * Hkv * (pl.mtiles / cx);   // clusters of one split
   const int64_t tot_tiles = ctx_tiles + tree_tiles;
-  // KV splits per (b, kvh, M-tile), up to a cluster of 16 (non-portable sizes
-  // above 8 count only where the device keeps such clusters resident): the
-  // count that minimises (waves of resident clusters) x (tiles per CTA + a
-  // fixed cost of about four tiles for set-up, first loads and the merge)
+  // KV splits per (b, kvh, M-tile or pair), up to a cluster of 16 CTAs
+  // (non-portable sizes above 8 count only where the device keeps such
+  // clusters resident): the count that minimises (waves of resident clusters)
+  // x (tiles per CTA + a fixed cost of about four tiles for set-up, first
+  // loads and the merge)
   int best = 1;
   double best_cost = 1e30;
-  for (int s = 1; s <= ATT_MAX_SPLITS; ++s) {
+  for (int s = 1; s <= max_splits; ++s) {
     if (s > 1 && tot_tiles < 2LL * s) break;
-    int per_wave = (s == 1) ? num_sms : max_active_clusters(d, paged, s);
+    int per_wave = (s == 1 && !pl.pair) ? num_sms : max_active_clusters(d, paged, pl.pair != 0, s);
     if (per_wave < 1) continue;
     const int64_t waves = (units + per_wave - 1) / per_wave;
     const double cost = static_cast<double>(waves) * ((s > 1 ? 4.0 : 3.0) + (tot_tiles + s - 1) / s);
@@ -898,41 +1092,36 @@ AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, i
   // 16-request batch of 512..8192-token contexts, 1 split 237 us, 2 splits
   // 199 us, 4 splits 187 us.
   if (paged) {
-    const int64_t want = (4LL * num_sms + units - 1) / units;
-    int s_bal = static_cast<int>(std::min<int64_t>(ATT_MAX_SPLITS, want));
+    const int64_t want = (4LL * num_sms / cx + units - 1) / units;
+    int s_bal = static_cast<int>(std::min<int64_t>(max_splits, want));
     while (s_bal > best && tot_tiles < 2LL * s_bal) --s_bal;
-    if (s_bal > best && max_active_clusters(d, paged, s_bal) >= 1) best = s_bal;
+    if (s_bal > best && max_active_clusters(d, paged, pl.pair != 0, s_bal) >= 1) best = s_bal;
   }
   pl.splits = best;
   pl.tiles_per_split = static_cast<int>((tot_tiles + best - 1) / best);
   if (pl.tiles_per_split == 0) pl.tiles_per_split = 1;
   // one partial slot per (b, kvh, M-tile, split) when the KV is split
-  pl.ws_bytes = best > 1 ? static_cast<size_t>(units) * best * (d / 4 + 1) * ATT_M * sizeof(float4) : 0;
+  pl.ws_bytes = best > 1 ? static_cast<size_t>(B) * Hkv * pl.mtiles * best * (d / 4 + 1) * ATT_M * sizeof(float4) : 0;
   pl.off_o = pl.off_ml = 0;
   return pl;
 }
 
 cudaError_t prepare_tree_attn() {
   cudaError_t e;
-  for (const void *fn : {reinterpret_cast<const void *>(tree_attn_tc_kernel<128, false>),
-                         reinterpret_cast<const void *>(tree_attn_tc_kernel<128, true>),
-                         reinterpret_cast<const void *>(tree_attn_tc_kernel<64, false>),
-                         reinterpret_cast<const void *>(tree_attn_tc_kernel<64, true>)}) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  const void *fns[6] = {attn_kernel_fn<false>(128, false), attn_kernel_fn<false>(128, true),
+                        attn_kernel_fn<false>(64, false),  attn_kernel_fn<false>(64, true),
+                        attn_kernel_fn<true>(128, false),  attn_kernel_fn<true>(128, true)};
+  const int smem[6] = {attn_smem_bytes(128, false), attn_smem_bytes(128, false), attn_smem_bytes(64, false),
+                       attn_smem_bytes(64, false),  attn_smem_bytes(128, true),  attn_smem_bytes(128, true)};
+  for (int i = 0; i < 6; ++i) {
+    e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i]);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fns[i], cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (e != cudaSuccess) return e;
   }
-  e = cudaFuncSetAttribute(tree_attn_tc_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnLayout<128>::SMEM);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tree_attn_tc_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnLayout<128>::SMEM);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tree_attn_tc_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnLayout<64>::SMEM);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tree_attn_tc_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnLayout<64>::SMEM);
-  if (e != cudaSuccess) return e;
-  if ((e = prefer_max_shared(tree_attn_tc_kernel<128, false>)) != cudaSuccess) return e;
-  if ((e = prefer_max_shared(tree_attn_tc_kernel<128, true>)) != cudaSuccess) return e;
-  if ((e = prefer_max_shared(tree_attn_tc_kernel<64, false>)) != cudaSuccess) return e;
-  if ((e = prefer_max_shared(tree_attn_tc_kernel<64, true>)) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tree_attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, f32_smem_bytes(128));
   if (e != cudaSuccess) return e;
   return prefer_max_shared(tree_attn_f32_kernel);
@@ -967,17 +1156,22 @@ cudaError_t launch_tree_attn_tc(const CUtensorMap *maps, const AttnPlan &pl, int
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.mtiles, pl.splits, B * Hkv);
   cfg.blockDim = dim3(ATT_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = d == 128 ? AttnLayout<128>::SMEM : AttnLayout<64>::SMEM;
+  cfg.dynamicSmemBytes = attn_smem_bytes(d, pl.pair != 0);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = fill_launch_attrs(attr, 1, pl.splits);   // the splits of one (b, kvh, M-tile) form a cluster
-  if (d == 128) {
-    if (paged) return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128, true>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
-    return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128, false>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  // the splits of one (b, kvh, M-tile) -- and the two CTAs of a pair -- form a cluster
+  cfg.numAttrs = fill_launch_attrs(attr, pl.pair ? 2 : 1, pl.splits);
+  if (pl.pair) {
+    if (paged) return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128, true, true>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128, false, true>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
   }
-  if (paged) return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<64, true>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
-  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<64, false>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  if (d == 128) {
+    if (paged) return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128, true, false>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128, false, false>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  }
+  if (paged) return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<64, true, false>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<64, false, false>, maps[0], maps[1], maps[2], maps[3], maps[4], p);
 }
 
 cudaError_t launch_tree_attn_f32(const float *q, const float *kt, const float *vt, const float *kc, const float *vc,
