@@ -41,10 +41,10 @@
  *   caller zeroes *dev_err and reads it after its own synchronisation.
  * - Calls on different streams are independent as long as they do not share
  *   output buffers or workspaces.
- * - The accept workspace must be zero-filled once when allocated; every call
- *   leaves it zero-filled again, so it can be reused without clearing.  The
- *   tree_attn workspace needs no initialisation.  Two calls in flight at the
- *   same time must not share a workspace.
+ * - The accept and tree_attn workspaces must be zero-filled once when
+ *   allocated; every call leaves them as it needs them, so they can be reused
+ *   without clearing.  Two calls in flight at the same time must not share a
+ *   workspace.
  */
 #ifndef BASTION_H
 #define BASTION_H
@@ -221,11 +221,15 @@ typedef struct {
 } bastion_kv_cache;
 
 /* Bytes of workspace bastion_tree_attn needs for these sizes on the current
- * device: when the context is split over several CTAs, one partial (O, m, l)
- * slot of 128 x (d + 4) floats per (request, KV head, 128-row tile, split);
- * 0 when it is not split.  The value depends on the device (SM count and
- * cluster occupancy), so query it on the device that runs the call.  Every
- * call overwrites the slots it reads; the content needs no initialisation. */
+ * device (bf16).  Contiguous cache: when the context is split over several
+ * CTAs, one partial (O, m, l) slot of 128 x (d + 4) floats per (request, KV
+ * head, 128-row tile, split), else 0.  Paged cache: one ticket word per
+ * (request, KV head, 128-row tile), then two partial slots per CTA of the
+ * grid (one CTA per SM).  The value depends on the device (SM count, cluster
+ * occupancy): query it on the device that runs the call.  The workspace must
+ * be zero-filled once when it is allocated; every call leaves it as the next
+ * one needs it (after a call that reported BASTION_DEVERR_TIMEOUT, zero it
+ * again).  The f32 path uses no workspace. */
 size_t bastion_tree_attn_workspace_size(int B, int n_max, int Hq, int Hkv, int d,
                                         const bastion_kv_cache *kv);
 
@@ -245,10 +249,14 @@ size_t bastion_tree_attn_workspace_size(int B, int n_max, int Hq, int Hkv, int d
  * dtype bf16: tensor-core path (tcgen05, fp32 softmax and accumulation);
  * dtype f32: exact fp32 path.  out has the input dtype; rows i >= n[b] are not
  * written.  Requires d in {64, 128}, Hq % Hkv == 0, n_max <= 256, base
- * pointers 16-byte aligned.  ws: device workspace of at least
- * bastion_tree_attn_workspace_size() bytes, 16-byte aligned (may be NULL when
- * that size is 0), else BASTION_ERR_WORKSPACE.  Device errors:
- * BASTION_DEVERR_N, _CTX, _PAGE, _TIMEOUT.
+ * pointers 16-byte aligned; bf16 with a paged cache: B <= 512.  ws: device
+ * workspace of at least bastion_tree_attn_workspace_size() bytes, 16-byte
+ * aligned, zero-filled when allocated (see there), else
+ * BASTION_ERR_WORKSPACE.  bf16 work: with a contiguous cache each (request,
+ * KV head, 128-row tile) streams its keys on one CTA or on a cluster of CTAs
+ * that split them; with a paged cache the batch's actual work (every
+ * request's KV heads x 128-row tiles x 128-key tiles) is split evenly over one
+ * CTA per SM.  Device errors: BASTION_DEVERR_N, _CTX, _PAGE, _TIMEOUT.
  */
 bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *v_tree,
                                  bastion_dtype dtype, int B, int n_max, int Hq, int Hkv, int d,

@@ -32,18 +32,15 @@ cudaError_t launch_accept(const void *target, bool bf16, int B, int n_max, int V
                           int32_t *acc_nodes, int32_t *acc_tok, int32_t *bonus, int32_t *argmax_out, void *ws,
                           uint32_t *dev_err, int num_sms, cudaStream_t stream);
 struct AttnPlan {
-  int mtiles, splits, tiles_per_split;
-  int pair;   // 1: CTA pairs (cta_group::2): K tensor maps load 64-key boxes
+  int paged, mtiles, splits, nctas;
   int64_t cap;
-  size_t ws_bytes, off_o, off_ml;
+  size_t ws_bytes, ticket_bytes;
 };
-AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, int num_sms, bool paged,
-                        int page_size);
+AttnPlan plan_tree_attn(int B, int n_max, int Hq, int Hkv, int d, int64_t cap, int num_sms, bool paged);
 cudaError_t launch_tree_attn_tc(const CUtensorMap *maps, const AttnPlan &pl, int B, int n_max, int Hq, int Hkv, int d,
-                                float scale, bool paged, int page_size, int max_pages, int num_pages,
-                                const int32_t *ctx_len, const int32_t *n, const uint64_t *mask,
-                                const int32_t *block_table, void *out, void *ws, uint32_t *dev_err,
-                                cudaStream_t stream);
+                                float scale, int page_size, int max_pages, int num_pages, const int32_t *ctx_len,
+                                const int32_t *n, const uint64_t *mask, const int32_t *block_table, void *out,
+                                void *ws, uint32_t *dev_err, cudaStream_t stream);
 cudaError_t launch_tree_attn_f32(const float *q, const float *kt, const float *vt, const float *kc, const float *vc,
                                  float *out, int B, int n_max, int Hq, int Hkv, int d, float scale, bool paged,
                                  int64_t L_max, int page_size, int max_pages, int num_pages, int64_t cap,
@@ -284,8 +281,7 @@ size_t bastion_tree_attn_workspace_size(int B, int n_max, int Hq, int Hkv, int d
   if (!kv || B < 1 || n_max < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (d != 64 && d != 128)) return 0;
   int sms = 0;
   if (current_device(&sms) != BASTION_OK) return 0;
-  return bst::plan_tree_attn(B, n_max, Hq, Hkv, d, kv_capacity(kv), sms, kv->block_table != nullptr, kv->page_size)
-      .ws_bytes;
+  return bst::plan_tree_attn(B, n_max, Hq, Hkv, d, kv_capacity(kv), sms, kv->block_table != nullptr).ws_bytes;
 }
 
 bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *v_tree, bastion_dtype dtype, int B,
@@ -329,9 +325,8 @@ bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *
   if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(kv->k) || !aligned16(kv->v) ||
       !aligned16(out))
     return fail(BASTION_ERR_INVALID_ARG, "tree_attn: bf16 tensors must be 16-byte aligned");
-  const bst::AttnPlan pl = bst::plan_tree_attn(B, n_max, Hq, Hkv, d, cap, sms, paged, kv->page_size);
-  // a CTA pair loads half the keys of every K tile per CTA
-  const cuuint32_t k_rows = pl.pair ? 64 : 128;
+  if (paged && B > 512) return fail(BASTION_ERR_UNSUPPORTED, "tree_attn: at most 512 requests per call (bf16, paged)");
+  const bst::AttnPlan pl = bst::plan_tree_attn(B, n_max, Hq, Hkv, d, cap, sms, paged);
   if (pl.ws_bytes > 0 && (!ws || ws_bytes < pl.ws_bytes || !aligned16(ws)))
     return fail(BASTION_ERR_WORKSPACE, "tree_attn: workspace too small (need " + std::to_string(pl.ws_bytes) + " bytes)");
 
@@ -344,13 +339,12 @@ bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(128 / g)};
     if (!encode_bf16(&maps[0], q, 3, dims, strides, box)) return fail(BASTION_ERR_CUDA, "tree_attn: Q tensor map");
   }
-  if (!paged) {  // K/V [B*Hkv][L_max][d]: box 64 x 128 x 1 (K of a CTA pair: 64 x 64 x 1)
+  if (!paged) {  // K/V [B*Hkv][L_max][d]: box 64 x 128 x 1
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kv->L_max),
                                 static_cast<cuuint64_t>(B) * Hkv};
     const cuuint64_t strides[2] = {d * es, static_cast<cuuint64_t>(kv->L_max) * d * es};
-    const cuuint32_t kbox[3] = {64, k_rows, 1};
     const cuuint32_t box[3] = {64, 128, 1};
-    if (!encode_bf16(&maps[1], kv->k, 3, dims, strides, kbox) || !encode_bf16(&maps[2], kv->v, 3, dims, strides, box))
+    if (!encode_bf16(&maps[1], kv->k, 3, dims, strides, box) || !encode_bf16(&maps[2], kv->v, 3, dims, strides, box))
       return fail(BASTION_ERR_CUDA, "tree_attn: KV tensor map");
   } else {  // pages [num_pages][Hkv][page_size][d]: box 64 x page_size x 1 x 1
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kv->page_size),
@@ -361,16 +355,15 @@ bastion_status bastion_tree_attn(const void *q, const void *k_tree, const void *
     if (!encode_bf16(&maps[1], kv->k, 4, dims, strides, box) || !encode_bf16(&maps[2], kv->v, 4, dims, strides, box))
       return fail(BASTION_ERR_CUDA, "tree_attn: paged KV tensor map");
   }
-  {  // tree K/V [B*n_max][Hkv][d]: box 64 x 1 x 128 (K of a CTA pair: 64 x 1 x 64)
+  {  // tree K/V [B*n_max][Hkv][d]: box 64 x 1 x 128
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hkv),
                                 static_cast<cuuint64_t>(B) * n_max};
     const cuuint64_t strides[2] = {d * es, static_cast<cuuint64_t>(Hkv) * d * es};
-    const cuuint32_t kbox[3] = {64, 1, k_rows};
     const cuuint32_t box[3] = {64, 1, 128};
-    if (!encode_bf16(&maps[3], k_tree, 3, dims, strides, kbox) || !encode_bf16(&maps[4], v_tree, 3, dims, strides, box))
+    if (!encode_bf16(&maps[3], k_tree, 3, dims, strides, box) || !encode_bf16(&maps[4], v_tree, 3, dims, strides, box))
       return fail(BASTION_ERR_CUDA, "tree_attn: tree KV tensor map");
   }
-  cudaError_t e = bst::launch_tree_attn_tc(maps, pl, B, n_max, Hq, Hkv, d, scale, paged, kv->page_size, kv->max_pages,
+  cudaError_t e = bst::launch_tree_attn_tc(maps, pl, B, n_max, Hq, Hkv, d, scale, kv->page_size, kv->max_pages,
                                            kv->num_pages, ctx_len, n, mask, kv->block_table, out, ws, dev_err, st);
   if (e != cudaSuccess) return cuda_fail(e, "tree_attn launch");
   return BASTION_OK;

@@ -88,6 +88,10 @@ BST_DEV void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar
 // every CTA of the cluster has started before touching its shared memory.
 BST_DEV void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
 BST_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// Full cluster barrier (every thread of every CTA), release / acquire.
+BST_DEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // L2 prefetch hints (no data returned to the SM, nothing to wait for).  A
 // kernel may issue them before its dependency wait: L2 is the point of
 // coherence, so a later write by the producing grid still wins, and the real
@@ -97,48 +101,6 @@ BST_DEV void prefetch_l2_bulk(const void *src, uint32_t bytes) {
 }
 BST_DEV void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
-}
-
-// ------------------------------------------------------------------ clusters / CTA pairs
-BST_DEV uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// shared::cluster address of the object at `p` (own shared memory) in CTA `rank`
-BST_DEV uint32_t mapa_shared(const void *p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-// Arrive on an mbarrier of any CTA of the cluster.  Default semantics
-// (release at CTA scope): what the arrival publishes here is TMEM written by
-// tcgen05.st, which the tcgen05 fences around the arrive/wait pair order; a
-// cluster-scope release adds a full memory barrier per arrival (measured: the
-// softmax warps' top stall reason) and orders nothing more that is needed.
-BST_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-// Full cluster barrier (every thread of every CTA), release / acquire.
-BST_DEV void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// TMA tensor loads for a CTA pair (cta_group::2): the data lands in this CTA's
-// shared memory, the completion is counted on the mbarrier at the
-// shared::cluster address `bar` (the pair's leader CTA's barrier).
-BST_DEV void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t bar, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-BST_DEV void tma_load_4d_pair(void *dst, const CUtensorMap *map, uint32_t bar, int c0, int c1, int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-      : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -174,45 +136,6 @@ BST_DEV void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t i
 // Arrive (once) on `bar` when every tcgen05.mma issued so far by this thread completed.
 BST_DEV void mma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-// CTA-pair forms (cta_group::2).  Allocation, permit release and deallocation
-// are collective: one warp of each CTA of the pair executes them.  The pair's
-// MMAs are issued by one thread of the leader (even) CTA: A rows 0..M/2-1 come
-// from the leader's shared memory (or TMEM), rows M/2..M-1 from the peer's at
-// the same offsets; B is split along N the same way; each CTA's TMEM receives
-// its M/2 rows of D, every column.
-BST_DEV void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)), "r"(ncols)
-               : "memory");
-}
-BST_DEV void tmem_relinquish_pair() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory"); }
-BST_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-BST_DEV void mma_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-BST_DEV void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive (once) on the mbarrier at the same shared-memory offset in every CTA
-// of `cta_mask` when every tcgen05.mma this thread issued so far completed.
-BST_DEV void mma_commit_pair(uint64_t *bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   smem_u32(bar)),
-               "h"(cta_mask)
                : "memory");
 }
 
