@@ -286,3 +286,30 @@ def test_topk_ties_between_signed_zeros():
     assert (s1["ids"][..., :5] == np.arange(5)).all()
     assert np.array_equal(np.signbit(s1["lg"].reshape(-1, 5)), np.signbit(o["lg"]))
     check_tree(tree, o["tree"])
+
+
+@pytest.mark.parametrize("dtype,V", [("f32", 262144), ("bf16", 262144), ("f32", 262143), ("bf16", 262140)])
+def test_topk_at_the_largest_vocabulary(dtype, V):
+    """V = 262144 and k = 32: every CTA of a row's cluster ranks its chunk
+    and the rank-0 merge takes the best 32 of them.  Row 0 is random (a heavy
+    upper tail), row 1 all equal (the exact-selection fallback in every
+    chunk), row 2 random with its maximum in the last element; odd V takes
+    the unaligned path."""
+    k, R = 32, 3
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((R, V)) * 3.0).astype(np.float32)
+    x[1] = 0.25
+    x[2, -1] = x[2].max() + 4.0
+    bits = I.store(x, dtype)
+    x = I.as_f32(bits, dtype)
+    want = dict(zip(("ids", "lg", "q", "lse"), oracle.topk_softmax(x, k)))
+    got = dict(ids=torch.empty(R, k, dtype=torch.int32, device="cuda"),
+               lg=torch.empty(R, k, dtype=torch.float32, device="cuda"),
+               q=torch.empty(R, k, dtype=torch.float32, device="cuda"),
+               lse=torch.empty(R, dtype=torch.float64, device="cuda"))
+    bn.bastion_topk_softmax(C.dev(bits, dtype), k, got["ids"], got["lg"], got["q"], got["lse"])
+    torch.cuda.synchronize()
+    wl = W["qwen3_8b_b1"].scaled(name="max_vocab", B=R, K=1, V=V, topk=k)
+    check_stage1(wl, {k_: v.cpu().numpy() for k_, v in got.items()}, want)
+    assert (got["ids"][1].cpu().numpy() == np.arange(k)).all()
+    assert int(got["ids"][2, 0]) == V - 1

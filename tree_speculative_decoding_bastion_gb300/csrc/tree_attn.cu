@@ -9,10 +9,15 @@
 // stage 2, self included):
 //     out = softmax(q . keys * scale) . values.
 //
-// bf16 path (tcgen05): one CTA per SM streams an equal share of the batch's
-// (request, KV head, 128-row M-tile) units, 128-key tiles at a time; the M
-// rows pack g = Hq/Hkv query heads x tree nodes of one KV head (GQA), so every
-// K/V tile is used by all heads of its group.  Details at the kernel.
+// bf16 path (tcgen05, S / P / O in tensor memory): the 128 M rows of a unit
+// pack g = Hq/Hkv query heads x tree nodes of one KV head (GQA), so every K/V
+// tile of 128 keys is used by all heads of its group.  Two kernels:
+//   * contiguous caches: one CTA per (request, KV head, M-tile, KV split),
+//     the splits of a unit forming a cluster that merges through L2;
+//   * paged caches: one CTA per SM streaming an equal share of the batch's
+//     concatenated tiles in gangs, units cut between gangs merged by the CTA
+//     that takes a unit's last ticket.
+// Details at each kernel.
 //
 // f32 path: an exact fp32 flash-decoding kernel, one CTA per (b, node, head),
 // 128-key blocks staged in shared memory.
@@ -926,7 +931,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_paged_kernel(
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kt,
     const __grid_constant__ CUtensorMap tm_vt, const PagedParams p) {
   using LY = PagedLayout<D>;
-  constexpr bool kPaged = true;
   constexpr int KS = LY::KSTAGES;
   constexpr int VS = LY::VSTAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -1062,9 +1066,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_paged_kernel(
       BST_TRACE_AT(2);
       constexpr int MAXPG = ATT_N / 8;          // page_size >= 8
       constexpr int PG_BEYOND = -2147483647 - 1;   // token past the context: read zeros
-      // page ids of the tile at cursor c (paged caches)
+      // page ids of the tile at cursor c
       auto fetch_pages = [&](const AttnCursor &c, bool valid, int (&pg)[MAXPG]) {
-        if (!kPaged) return;
         const int ps = p.page_size;
 #pragma unroll
         for (int pi = 0; pi < MAXPG; ++pi) {
@@ -1075,29 +1078,24 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_paged_kernel(
         }
       };
       // one K or V tile (context or tree) at cursor c into `dst`, completing
-      // on `fb`; pg: the tile's page ids (paged context tiles)
+      // on `fb`; pg: the tile's page ids (context tiles)
       auto load_tile = [&](const AttnCursor &c, bool is_v, uint8_t *dst, uint64_t *fb, const int (&pg)[MAXPG]) {
         const CUtensorMap *mc = is_v ? &tm_v : &tm_k;
         const CUtensorMap *mt = is_v ? &tm_vt : &tm_kt;
         if (c.t < c.rq.ctx_tiles) {
-          if (!kPaged) {
+          const int ps = p.page_size;
 #pragma unroll
-            for (int h = 0; h < LY::NH; ++h) tma_load_3d(dst + h * ATT_HALF, mc, fb, h * 64, c.t * ATT_N, c.b * p.Hkv + c.kvh);
-          } else {
-            const int ps = p.page_size;
-#pragma unroll
-            for (int pi = 0; pi < MAXPG; ++pi) {
-              if (pi * ps >= ATT_N) break;
-              int page = pg[pi];
-              if (page == PG_BEYOND) {
-                page = p.num_pages;   // out of range: the copy reads zeros
-              } else if (page < 0 || page >= p.num_pages) {
-                set_err(p.dev_err, BASTION_DEVERR_PAGE);
-                page = p.num_pages;
-              }
-#pragma unroll
-              for (int h = 0; h < LY::NH; ++h) tma_load_4d(dst + h * ATT_HALF + pi * ps * 128, mc, fb, h * 64, 0, c.kvh, page);
+          for (int pi = 0; pi < MAXPG; ++pi) {
+            if (pi * ps >= ATT_N) break;
+            int page = pg[pi];
+            if (page == PG_BEYOND) {
+              page = p.num_pages;   // out of range: the copy reads zeros
+            } else if (page < 0 || page >= p.num_pages) {
+              set_err(p.dev_err, BASTION_DEVERR_PAGE);
+              page = p.num_pages;
             }
+#pragma unroll
+            for (int h = 0; h < LY::NH; ++h) tma_load_4d(dst + h * ATT_HALF + pi * ps * 128, mc, fb, h * 64, 0, c.kvh, page);
           }
         } else {
           const int tt = c.t - c.rq.ctx_tiles;
@@ -1130,16 +1128,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_paged_kernel(
         // the stage is free once S(j - KS), which read it, is complete
         if (j >= KS && !mbar_wait(&bars->k_empty[st], ((j / KS) - 1) & 1, abort, ATT_WAIT_NS)) return false;
         mbar_expect_tx(&bars->k_full[st], LY::KV_BYTES);
-        if (kPaged) {
 #pragma unroll
-          for (int pi = 0; pi < MAXPG; ++pi) {
-            pgA[pi] = pgB[pi];
-            pgB[pi] = pgN[pi];
-          }
-          if (j + 1 < T) {
-            cursor_next(cn, p);
-            fetch_pages(cn, true, pgN);
-          }
+        for (int pi = 0; pi < MAXPG; ++pi) {
+          pgA[pi] = pgB[pi];
+          pgB[pi] = pgN[pi];
+        }
+        if (j + 1 < T) {
+          cursor_next(cn, p);
+          fetch_pages(cn, true, pgN);
         }
         load_tile(ck, false, smem + LY::K_OFF + st * LY::KV_BYTES, &bars->k_full[st], pgB);
         if (j < 8) BST_TRACE_AT(32 + j);
