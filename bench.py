@@ -42,10 +42,12 @@ DEFAULT_WORKLOAD = "long_ctx_b4"
 # dram__bytes_write.sum, one capture of the workload); an entry counts only
 # while the kernel's sources still hash to `src`
 KNOWN_TRAFFIC = {
-    ("topk_softmax", "qwen3_8b_b1"): {"bytes": 4899840, "src": "3f36d2757b948f0c"},
-    ("tree_build", "qwen3_8b_b1"): {"bytes": 28672, "src": "b1b8d9acb140e26c"},
-    ("tree_attn", "qwen3_8b_b1"): {"bytes": 17638400, "src": "db832ca8b3373a81"},
-    ("accept", "qwen3_8b_b1"): {"bytes": 19476736, "src": "fa0f3decba794f09"}
+    ("topk_softmax", "long_ctx_b4"): {"bytes": 19487232, "src": "4df76374a6957a55"},
+    ("tree_attn", "long_ctx_b4"): {"bytes": 547680512, "src": "4a7b1d5bd679bcb8"},
+    ("accept", "long_ctx_b4"): {"bytes": 159899648, "src": "cc63049a9c8293a7"},
+    ("topk_softmax", "llama31_8b_b16_paged"): {"bytes": 66130432, "src": "4df76374a6957a55"},
+    ("tree_attn", "llama31_8b_b16_paged"): {"bytes": 295165184, "src": "4a7b1d5bd679bcb8"},
+    ("accept", "llama31_8b_b16_paged"): {"bytes": 51021312, "src": "cc63049a9c8293a7"},
 }
 KERNEL_SOURCES = {
     "topk_softmax": ("topk_softmax.cu", "sm100_ptx.cuh", "common.cuh"),
