@@ -48,6 +48,11 @@ KNOWN_TRAFFIC = {
     ("topk_softmax", "llama31_8b_b16_paged"): {"bytes": 66130432, "src": "4df76374a6957a55"},
     ("tree_attn", "llama31_8b_b16_paged"): {"bytes": 295165184, "src": "4a7b1d5bd679bcb8"},
     ("accept", "llama31_8b_b16_paged"): {"bytes": 51021312, "src": "cc63049a9c8293a7"},
+    ("topk_softmax", "qwen3_8b_b1"): {"bytes": 4900864, "src": "4df76374a6957a55"},
+    ("tree_build", "qwen3_8b_b1"): {"bytes": 29440, "src": "48ae66f3c4acd9a7"},
+    ("tree_attn", "qwen3_8b_b1"): {"bytes": 17633792, "src": "4a7b1d5bd679bcb8"},
+    ("accept", "qwen3_8b_b1"): {"bytes": 19478784, "src": "cc63049a9c8293a7"},
+    ("tree_build", "long_ctx_b4"): {"bytes": 34048, "src": "48ae66f3c4acd9a7"},
 }
 KERNEL_SOURCES = {
     "topk_softmax": ("topk_softmax.cu", "sm100_ptx.cuh", "common.cuh"),
