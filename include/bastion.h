@@ -217,7 +217,7 @@ typedef struct {
   const int32_t *block_table; /* paged: [B, max_pages] page ids (device); contiguous: NULL */
   int max_pages;              /* paged: columns of block_table */
   int num_pages;              /* paged: pages in the pool */
-  int page_size;              /* paged: tokens per page (16) */
+  int page_size;              /* paged: tokens per page: 8, 16, 32, 64 or 128 */
 } bastion_kv_cache;
 
 /* Bytes of workspace bastion_tree_attn needs for these sizes on the current
