@@ -314,7 +314,8 @@ def time_oracle(wl, inp, steps, warmup, seconds=None):
                 break
     finally:
         ob.close()
-    return {"steps": len(walls), "wall_s": sum(walls), "full_s": sum(fulls), "value": len(fulls) / sum(fulls),
+    return {"steps": len(walls), "warmup": warmup, "wall_s": sum(walls), "full_s": sum(fulls),
+            "value": len(fulls) / sum(fulls),
             "cores": ob.P, "one_core_value": 1.0 / one_full, "one_core_wall_s": one_wall,
             "sample": ob.describe(), "cpu_model": host_cpu_model()}
 
@@ -330,7 +331,7 @@ def run_reference(args, rank, world):
     cpu = {"value": value, "unit": "steps/s", "cores": r["cores"], "kind": "oracle", "sample": r["sample"],
            "one_core": {"value": r["one_core_value"], "unit": "steps/s", "cores": 1}, "cpu_model": r["cpu_model"]}
     line = {"impl": "reference", "metric": "spec-tree steps/s", "value": value, "unit": "steps/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "n_gpus": world, "steps": r["steps"], "warmup": r["warmup"],
             "ms_per_step": 1000.0 * r["wall_s"] / r["steps"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(wl, "oracle on host cores"), "cpu_baseline": cpu,

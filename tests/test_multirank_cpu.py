@@ -80,3 +80,20 @@ def test_reference_arm_line_on_rank_zero():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_runs_the_steps_it_is_given():
+    """The reference arm times exactly --steps steps after --warmup untimed
+    ones (the counts in the line are the ones it ran), and reports the
+    all-cores figure with its core count beside a one-core figure."""
+    import json
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "tiny_v1024_f32", "--steps", "3", "--warmup", "2"], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["steps"] == 3 and line["warmup"] == 2
+    cpu = line["cpu_baseline"]
+    assert cpu["cores"] >= 1 and cpu["one_core"]["cores"] == 1 and cpu["one_core"]["value"] > 0
+    assert "model" in line["value_model"] and line["ms_per_step"] > 0
