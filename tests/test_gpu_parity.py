@@ -144,7 +144,7 @@ def attn_tol(wl):
     return (2e-2, 1e-2) if wl.dtype == "bf16" else (1e-4, 1e-4)
 
 
-def _attention_parity(inp, tree, max_rows, kv=None):
+def _attention_parity(inp, tree, max_rows, kv=None, rows=None):
     wl = inp.wl
     kv = C.kv_of(inp) if kv is None else kv
     out = torch.full((wl.B, wl.n_max, wl.Hq, wl.d), float("nan"), device="cuda",
@@ -159,7 +159,8 @@ def _attention_parity(inp, tree, max_rows, kv=None):
     assert int(err.item()) == 0
     got = out.float().cpu().numpy()
     total = int(tree["n"].sum()) * wl.Hq
-    rows = None if total <= max_rows else C.attention_rows(inp, tree, max_rows)
+    if rows is None and total > max_rows:
+        rows = C.attention_rows(inp, tree, max_rows)
     want = C.oracle_attention(inp, tree, rows=rows)
     if rows is None:
         rows = [(b, i, h) for b in range(wl.B) for i in range(int(tree["n"][b])) for h in range(wl.Hq)]
@@ -236,6 +237,27 @@ def test_attention_and_whole_step_match_oracle(name):
     atol, rtol = attn_tol(wl)
     for r in rows:
         assert np.all(np.abs(got[r] - want[r]) <= atol + rtol * np.abs(want[r])), r
+
+
+def test_long_context_attention_covers_every_head_group_and_m_tile():
+    """long_ctx_b4 at full size (4 requests x 32K context, 128 nodes, GQA 32/8):
+    rows from every (request, KV head) pair and from each of its four
+    128-row M-tiles (nodes 0-31, 32-63, 64-95, 96-127; the M rows pack the
+    group's four query heads node by node), each with a different head of the
+    group, against the oracle."""
+    wl = W["long_ctx_b4"]
+    inp, o = C.pick(wl, 0)
+    tree = o["tree"]
+    nodes_per_tile = 128 // wl.g
+    rows = []
+    for b in range(wl.B):
+        nb = int(tree["n"][b])
+        for kvh in range(wl.Hkv):
+            for m in range((nb * wl.g + 127) // 128):
+                i = min(nb - 1, nodes_per_tile * m + (7 * (b + kvh) + 5 * m) % nodes_per_tile)
+                rows.append((b, i, kvh * wl.g + (b + kvh + m) % wl.g))
+    assert len({(b, h // wl.g) for b, _, h in rows}) == wl.B * wl.Hkv
+    _attention_parity(inp, tree, max_rows=0, rows=sorted(set(rows)))
 
 
 def _fill_host(views, inp, target):
