@@ -42,7 +42,7 @@ SMALL = {
                                                   n_min=60, n_max=64),
     "paged_p128": W["llama31_8b_b16_paged"].scaled(name="paged_p128", B=2, V=4096, L=800, L_min=129, page_size=128,
                                                    n_min=50, n_max=64),
-    "pair_3tiles": W["qwen3_8b_b1"].scaled(name="pair_3tiles", B=2, V=4096, K=8, L=333, n_min=96, n_max=96),
+    "three_mtiles": W["qwen3_8b_b1"].scaled(name="three_mtiles", B=2, V=4096, K=8, L=333, n_min=96, n_max=96),
 }
 FULL = ["tiny_v1024_f32", "qwen3_8b_b1", "llama31_8b_b16_paged", "long_ctx_b4", "controller_sweep_peaked",
         "controller_sweep_flat"]
