@@ -77,6 +77,8 @@ typedef enum { BASTION_F32 = 0, BASTION_BF16 = 1 } bastion_dtype;
 #define BASTION_DEVERR_CTX 0x4u   /* ctx_len[b] < 0 or beyond the KV cache capacity */
 #define BASTION_DEVERR_PAGE 0x8u  /* a block-table page id outside [0, num_pages) */
 #define BASTION_DEVERR_TIMEOUT 0x10u /* a bounded in-kernel wait expired (the call's outputs are invalid) */
+#define BASTION_DEVERR_LAYOUT 0x20u  /* a kernel found its shared memory misaligned and did nothing
+                                       (not expected on sm_103; the call's outputs are invalid) */
 
 /* Limits of this build. */
 #define BASTION_MAX_TOPK 32     /* k of the top-k */

@@ -288,7 +288,8 @@ struct SplitBars {
   uint64_t drain;
   uint64_t xbar[4];                   // half-row max / sum swaps of warps q and q + 4
   float xmax[2][2][ATT_M];
-  float xl[2][ATT_M];
+  // (the row sums' swap at the end, [column half][row], uses the first K
+  // stage: by then every MMA has read its last K tile)
   uint32_t tmem_base;
   int abort;
 };
@@ -297,16 +298,21 @@ template <int D>
 struct SplitLayout {
   static constexpr int NH = D / 64;
   static constexpr int KSTAGES = ATT_SBUF;   // K stage j mod 3 is S buffer j mod 3 (one barrier serves both)
-  // (head_dim 128 keeps two V tiles: three do not fit next to three K tiles,
-  // Q and the barriers)
-  static constexpr int VSTAGES = D == 128 ? 2 : 3;
+  // Three V stages too: with two, the copy of V(j) could start only once
+  // P V(j - 2) had freed its stage, so a tile took at least half a load
+  // latency.  With head_dim 128 the seven 32 KB tiles leave 3 KB of the
+  // 227 KB for the barriers, so the dynamic shared memory is used unpadded
+  // (its base is 1024-byte aligned: the kernel has no static shared memory)
+  // and the row sums swap through a K stage at the end.
+  static constexpr int VSTAGES = 3;
   static constexpr int KV_BYTES = NH * ATT_HALF;
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = NH * ATT_HALF;
   static constexpr int V_OFF = K_OFF + KSTAGES * KV_BYTES;
   static constexpr int BAR_OFF = V_OFF + VSTAGES * KV_BYTES;
   static constexpr int USED = BAR_OFF + static_cast<int>(sizeof(SplitBars));
-  static constexpr int SMEM = (USED + 1024) > 120 * 1024 ? (USED + 1024) : 120 * 1024;
+  // at least 120 KB so that a single CTA owns each SM (its TMEM allocation is 512 columns)
+  static constexpr int SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
   static_assert(SMEM <= 227 * 1024, "exceeds the shared memory of one CTA");
 };
 
@@ -393,9 +399,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_split_kernel(
   constexpr int KS = LY::KSTAGES;
   constexpr int VS = LY::VSTAGES;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // the 128-byte swizzled TMA tiles need a 1024-byte aligned base, which the
+  // unpadded layout takes as given; a misaligned base is reported, not used
+  if ((smem_u32(smem_raw) & 1023u) != 0u) {
+    if (threadIdx.x == 0) set_err(p.dev_err, BASTION_DEVERR_LAYOUT);
+    return;
+  }
+  uint8_t *smem = smem_raw;
   uint8_t *sQ = smem + LY::Q_OFF;
   SplitBars *bars = reinterpret_cast<SplitBars *>(smem + LY::BAR_OFF);
+  float *xl = reinterpret_cast<float *>(smem + LY::K_OFF);   // [2][ATT_M], used after the last MMA
   volatile int *abort = &bars->abort;
 
   const int mtile = blockIdx.x;
@@ -665,10 +678,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) tree_attn_split_kernel(
       // after every MMA of this CTA); the two halves' row sums add
       if (ok && !warp_wait(&bars->drain, 0, abort)) ok = false;
       if (tid == 0) BST_TRACE_AT(27);
-      bars->xl[ch][r] = l_run;
+      xl[ch * ATT_M + r] = l_run;
       mbar_arrive(xb);
       if (ok && !warp_wait(xb, T & 1, abort)) ok = false;
-      const float l_row = l_run + bars->xl[ch ^ 1][r];
+      const float l_row = l_run + xl[(ch ^ 1) * ATT_M + r];
       float o[DH];
       if (ok) {
         tc_fence_after();
