@@ -51,7 +51,7 @@ def test_version_and_status_strings(L):
 def test_error_word_helpers(L):
     from tree_speculative_decoding_bastion_gb300 import binding as bn
     assert L.bastion_error_status(0) == OK
-    for bit in (bn.DEVERR_TOKEN, bn.DEVERR_N, bn.DEVERR_CTX, bn.DEVERR_PAGE):
+    for bit in (bn.DEVERR_TOKEN, bn.DEVERR_N, bn.DEVERR_CTX, bn.DEVERR_PAGE, bn.DEVERR_LAYOUT):
         assert L.bastion_error_status(bit) == DEVICE
     assert L.bastion_error_status(bn.DEVERR_TIMEOUT) == TIMEOUT
     assert L.bastion_error_status(bn.DEVERR_TIMEOUT | bn.DEVERR_N) == TIMEOUT

@@ -24,6 +24,7 @@ DEVERR_N = 0x2
 DEVERR_CTX = 0x4
 DEVERR_PAGE = 0x8
 DEVERR_TIMEOUT = 0x10
+DEVERR_LAYOUT = 0x20
 
 _c_int, _c_i64, _c_f, _c_p, _c_sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 
