@@ -189,22 +189,26 @@ BST_DEV float softmax_load_mask_max(uint32_t taddr, bool is_ctx, int nvalid, uns
 }
 
 // P = 2^(S cs - msub) as bf16 pairs into TMEM at taddr_p (32 columns), and
-// the sum of this half-row's P (before rounding).
+// the sum of this half-row's P (before rounding).  The softmax warps are
+// bound by instruction issue, so the scale-and-offset and the sums run on
+// packed fp32 pairs (FFMA2, FADD2): long_ctx_b4 attention 271 -> 253 us.
 BST_DEV float softmax_exp_store(const uint32_t (&s)[ATT_N / 2], float cs, float msub, uint32_t taddr_p) {
   constexpr int HC = ATT_N / 2;
-  float sum[8];
+  float2 sum[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+  for (int i = 0; i < 4; ++i) sum[i] = make_float2(0.f, 0.f);
   uint32_t pk[HC / 2];
+  const float2 cs2 = make_float2(cs, cs), ms2 = make_float2(-msub, -msub);
 #pragma unroll
   for (int c = 0; c < HC; c += 2) {
-    const float p0 = ex2(fmaf(__uint_as_float(s[c]), cs, -msub));
-    const float p1 = ex2(fmaf(__uint_as_float(s[c + 1]), cs, -msub));
-    sum[(c >> 1) & 7] += p0 + p1;
+    const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), cs2, ms2);
+    const float p0 = ex2(x.x);
+    const float p1 = ex2(x.y);
+    sum[(c >> 1) & 3] = __fadd2_rn(sum[(c >> 1) & 3], make_float2(p0, p1));
     pk[c >> 1] = pack_bf16x2(p0, p1);
   }
   tmem_st32(taddr_p, pk);
-  return ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+  return ((sum[0].x + sum[1].x) + (sum[2].x + sum[3].x)) + ((sum[0].y + sum[1].y) + (sum[2].y + sum[3].y));
 }
 
 // O *= alpha on this warp's DH columns of its rows.
