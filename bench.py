@@ -43,14 +43,14 @@ DEFAULT_WORKLOAD = "long_ctx_b4"
 # while the kernel's sources still hash to `src`
 KNOWN_TRAFFIC = {
     ("topk_softmax", "long_ctx_b4"): {"bytes": 19487488, "src": "cf7c9111dc12f3bb"},
-    ("tree_attn", "long_ctx_b4"): {"bytes": 547865344, "src": "0c9da3e9f2b8fdd9"},
+    ("tree_attn", "long_ctx_b4"): {"bytes": 548102144, "src": "abb308e9ee576ad9"},
     ("accept", "long_ctx_b4"): {"bytes": 159599872, "src": "46cf3ac181492cfd"},
     ("topk_softmax", "llama31_8b_b16_paged"): {"bytes": 66237696, "src": "cf7c9111dc12f3bb"},
-    ("tree_attn", "llama31_8b_b16_paged"): {"bytes": 294968320, "src": "0c9da3e9f2b8fdd9"},
+    ("tree_attn", "llama31_8b_b16_paged"): {"bytes": 295353856, "src": "abb308e9ee576ad9"},
     ("accept", "llama31_8b_b16_paged"): {"bytes": 50337024, "src": "46cf3ac181492cfd"},
     ("topk_softmax", "qwen3_8b_b1"): {"bytes": 4905216, "src": "cf7c9111dc12f3bb"},
     ("tree_build", "qwen3_8b_b1"): {"bytes": 29440, "src": "48ae66f3c4acd9a7"},
-    ("tree_attn", "qwen3_8b_b1"): {"bytes": 17643008, "src": "0c9da3e9f2b8fdd9"},
+    ("tree_attn", "qwen3_8b_b1"): {"bytes": 17634048, "src": "abb308e9ee576ad9"},
     ("accept", "qwen3_8b_b1"): {"bytes": 19477760, "src": "46cf3ac181492cfd"},
     ("tree_build", "long_ctx_b4"): {"bytes": 34048, "src": "48ae66f3c4acd9a7"},
 }
