@@ -11,6 +11,9 @@ HBM), bracketed by a barrier and device syncs, timed with CUDA events on the
 launching stream; max over ranks.  Per-kernel durations for the roofline come
 from a second pass: each stage launched back to back over the input sets
 between two events, queued behind a GPU sleep so host launch gaps do not count.
+The line also carries the same steps launched eagerly (no graph, the host's
+launch cost included) and the step's roofline: the per-stage minimum times at
+the measured peaks, summed, over the measured step time.
 With N > 1 (torchrun) every rank is an independent replica on its own inputs.
 """
 import os
@@ -444,6 +447,22 @@ def attn_flops(wl, inp, n, depth):
     return f
 
 
+def step_roofline(sb, flops, hbm_gbs, tensor_tflops, step_us):
+    """The step's roofline: the sum of the per-stage minimum times at the peaks
+    (each input read once; attention at the larger of its HBM and tensor
+    times, HBM alone without a tensor-core count; the tree build, a serial
+    chain, has no throughput roofline and counts zero), and that sum over the
+    measured step time."""
+    t = {"topk_softmax": sb["topk_softmax"] / (hbm_gbs * 1e9), "accept": sb["accept"] / (hbm_gbs * 1e9)}
+    t_attn = sb["tree_attn"] / (hbm_gbs * 1e9)
+    if flops is not None:
+        t_attn = max(t_attn, flops / (tensor_tflops * 1e12))
+    t["tree_attn"] = t_attn
+    min_us = sum(t.values()) * 1e6
+    return {"min_us": min_us, "measured_us": step_us, "frac": min_us / step_us,
+            "per_stage_min_us": {k: v * 1e6 for k, v in t.items()}}
+
+
 def tree_report(step):
     """Per request of the last step run: the chosen tree size n, A_hat(T_n),
     S(n), the accepted length and the tokens the step emits (accepted + bonus)."""
@@ -568,6 +587,32 @@ def run_ours(args, rank, world, local_rank):
     ms = max_over_ranks(e0.elapsed_time(e1), world)
     assert int(step.dev_err.item()) == 0, "device error word set during the benchmark"
 
+    # ---- the same steps launched eagerly: the four calls of every step issued
+    # from the host one by one (no graph), the host's launch cost included;
+    # each input set's calls are checked and marshalled once (prepare)
+    n_eager = min(args.steps, 2000)
+    with torch.cuda.stream(stream):
+        prepared = [step.prepare(*args_of(s)) for s in sets]
+        for i in range(3):
+            prepared[i % len(sets)]()
+    torch.cuda.synchronize()
+    barrier()
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        ev_e[0].record(stream)
+        for i in range(n_eager):
+            prepared[i % len(sets)]()
+        ev_e[1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    eager_ms = max_over_ranks(ev_e[0].elapsed_time(ev_e[1]), world)
+    assert int(step.dev_err.item()) == 0, "device error word set during the eager steps"
+    eager = {"value": job_throughput(world, n_eager, eager_ms), "unit": "steps/s", "steps": n_eager,
+             "ms_per_step": eager_ms / n_eager,
+             "note": "the same rotating input sets, each step's four library calls launched from the host "
+                     "(SpecTreeStep.prepare: arguments checked and marshalled once per input set; programmatic "
+                     "launch between the kernels, no CUDA graph); CUDA events on the launching stream"}
+
     # ---- per-kernel durations: each stage launched back to back over the
     # rotating input sets (2 passes) between two events on the launching
     # stream, the way the stages follow one another inside a step (the
@@ -646,6 +691,10 @@ def run_ours(args, rank, world, local_rank):
             e["TFLOP/s"] = fl / (us[k] * 1e-6) / 1e12
             e["tensor_frac"] = e["TFLOP/s"] / tf_burst
         stages[k] = e
+
+    step_roof = step_roofline(sb, fl, hbm, tf_burst, ms / args.steps * 1e3)
+    step_roof["note"] = ("per-stage minimum times at the measured peaks (HBM copy, burst bf16 GEMM) for set 0's "
+                         "trees; the tree build counts zero")
 
     # ---- beyond the step: commit the accepted path of set 0 to a scratch
     # cache laid out like the workload's (contiguous rows with room, or fresh
@@ -825,6 +874,7 @@ def run_ours(args, rank, world, local_rank):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf else "f32",
                 "data": "synthetic", "config": config_of(wl, l2), "roofline": roof, "stages": stages,
+                "step_roofline": step_roof, "eager": eager,
                 "cpu_baseline": cpu, "e2e": e2e, "next_rows": {"kv_commit": commit, "drafter_attention": drafter,
                                                       "tree_build_threshold": pruned,
                                                       "latency_calibration": calib},

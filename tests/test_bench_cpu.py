@@ -43,3 +43,16 @@ def test_attention_flops_by_hand():
     per_key = 32 * 4 * 128
     keys = (10 + 1) + (10 + 2) + (10 + 3) + (7 + 1) + (7 + 2)
     assert f == per_key * keys
+
+
+def test_step_roofline_sums_the_stage_minima():
+    # 1 GB/s and 1 TFLOP/s peaks make every minimum time readable by eye
+    sb = {"topk_softmax": 2000, "tree_attn": 3000, "accept": 5000}
+    b = bench()
+    r = b.step_roofline(sb, None, 1.0, 1.0, 20.0)             # no tensor count: attention at HBM
+    assert r["per_stage_min_us"] == {"topk_softmax": 2.0, "accept": 5.0, "tree_attn": 3.0}
+    assert r["min_us"] == 10.0 and r["frac"] == 0.5
+    r = b.step_roofline(sb, 7e6, 1.0, 1.0, 20.0)              # 7 us of tensor work binds attention
+    assert r["per_stage_min_us"]["tree_attn"] == 7.0 and r["min_us"] == 14.0
+    r = b.step_roofline(sb, 1e6, 1.0, 1.0, 20.0)              # 1 us of tensor work: HBM still binds
+    assert r["per_stage_min_us"]["tree_attn"] == 3.0

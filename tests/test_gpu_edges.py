@@ -313,3 +313,31 @@ def test_topk_at_the_largest_vocabulary(dtype, V):
     check_stage1(wl, {k_: v.cpu().numpy() for k_, v in got.items()}, want)
     assert (got["ids"][1].cpu().numpy() == np.arange(k)).all()
     assert int(got["ids"][2, 0]) == V - 1
+
+
+def test_prepared_step_launches_on_call_and_matches_the_oracle():
+    """SpecTreeStep.prepare checks and marshals the four calls once and
+    launches nothing; each call of the prepared step then runs the whole step
+    on the inputs' current contents (here: the controller's S(N) stop, bf16)."""
+    wl = W["controller_sweep_flat"].scaled(name="prepared", B=3, V=12288, n_min=2, n_max=48, L=200)
+    inp, o = C.pick(wl, 0)
+    tree = o["tree"]
+    target = C.target_for(inp, tree)
+    kv = C.kv_of(inp)
+    step = bn.SpecTreeStep(wl.B, wl.K, wl.V, wl.topk, wl.n_min, wl.n_max, wl.Hq, wl.Hkv, wl.d, kv,
+                           act_dtype=torch.bfloat16)
+    Ct = None if inp.C is None else C.dev(inp.C)
+    args = (C.dev(inp.logits, wl.dtype), C.dev(inp.root_tok), C.dev(inp.ctx_len), Ct, inp.L_AR,
+            C.dev(inp.q, wl.dtype), C.dev(inp.k_tree, wl.dtype), C.dev(inp.v_tree, wl.dtype), kv, inp.scale,
+            C.dev(target, wl.dtype))
+    step.result.fill_(-7)
+    prepared = step.prepare(*args)
+    torch.cuda.synchronize()
+    assert (step.result.cpu().numpy() == -7).all()    # nothing ran yet
+    for _ in range(2):                                # repeatable on the same workspaces
+        step.result.fill_(-7)
+        prepared()
+        torch.cuda.synchronize()
+        compare_step(inp, tree, target, step)
+    with pytest.raises(bn.BastionError):              # checks still run when preparing
+        step.prepare(*args[:5], args[5].float(), *args[6:])

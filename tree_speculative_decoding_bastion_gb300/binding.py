@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from dataclasses import dataclass
 from typing import Optional
 
@@ -97,6 +98,22 @@ def _check(status: int, what: str) -> None:
                            f"({L.bastion_last_error().decode()})")
 
 
+# While a step is being prepared (SpecTreeStep.prepare), the stage functions
+# record their marshalled calls here instead of issuing them.
+_rec = threading.local()
+
+
+def _call(name: str, *args) -> None:
+    """Issue library call `name` with its marshalled arguments, or record it
+    when a step is being prepared on this thread."""
+    fn = getattr(lib(), name)
+    calls = getattr(_rec, "calls", None)
+    if calls is not None:
+        calls.append((fn, args, name))
+        return
+    _check(fn(*args), name)
+
+
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -165,9 +182,8 @@ def bastion_topk_softmax(logits: torch.Tensor, k: int, ids, lg, q, lse, dev_err=
         raise BastionError("lse must hold one value per row")
     if dev_err is not None:
         _need(dev_err, torch.int32, (1,), "dev_err")
-    _check(lib().bastion_topk_softmax(_ptr(flat), _dtype_code(logits), rows, V, row_stride, int(k), _ptr(ids),
-                                      _ptr(lg), _ptr(q), _ptr(lse), _ptr(dev_err), _stream(stream)),
-           "bastion_topk_softmax")
+    _call("bastion_topk_softmax", _ptr(flat), _dtype_code(logits), rows, V, row_stride, int(k), _ptr(ids), _ptr(lg),
+          _ptr(q), _ptr(lse), _ptr(dev_err), _stream(stream))
 
 
 def bastion_tree_build(ids, lg, lse, V: int, root_tok, ctx_len, n_min: int, n_max: int, C: Optional[torch.Tensor],
@@ -197,17 +213,14 @@ def bastion_tree_build(ids, lg, lse, V: int, root_tok, ctx_len, n_min: int, n_ma
     if dev_err is not None:
         _need(dev_err, torch.int32, (1,), "dev_err")
     if tau:
-        _check(lib().bastion_tree_build_threshold(_ptr(ids), _ptr(lg), _ptr(lse), B, K, k, int(V), _ptr(root_tok),
-                                                  _ptr(ctx_len), int(n_min), int(n_max), _ptr(C), float(L_AR),
-                                                  float(tau), _ptr(n), _ptr(parent), _ptr(token), _ptr(depth),
-                                                  _ptr(pos), _ptr(rho), _ptr(mask), _ptr(ahat), _ptr(S),
-                                                  _ptr(S_curve), _ptr(dev_err), _stream(stream)),
-               "bastion_tree_build_threshold")
+        _call("bastion_tree_build_threshold", _ptr(ids), _ptr(lg), _ptr(lse), B, K, k, int(V), _ptr(root_tok),
+              _ptr(ctx_len), int(n_min), int(n_max), _ptr(C), float(L_AR), float(tau), _ptr(n), _ptr(parent),
+              _ptr(token), _ptr(depth), _ptr(pos), _ptr(rho), _ptr(mask), _ptr(ahat), _ptr(S), _ptr(S_curve),
+              _ptr(dev_err), _stream(stream))
         return
-    _check(lib().bastion_tree_build(_ptr(ids), _ptr(lg), _ptr(lse), B, K, k, int(V), _ptr(root_tok), _ptr(ctx_len),
-                                    int(n_min), int(n_max), _ptr(C), float(L_AR), _ptr(n), _ptr(parent), _ptr(token),
-                                    _ptr(depth), _ptr(pos), _ptr(rho), _ptr(mask), _ptr(ahat), _ptr(S),
-                                    _ptr(S_curve), _ptr(dev_err), _stream(stream)), "bastion_tree_build")
+    _call("bastion_tree_build", _ptr(ids), _ptr(lg), _ptr(lse), B, K, k, int(V), _ptr(root_tok), _ptr(ctx_len),
+          int(n_min), int(n_max), _ptr(C), float(L_AR), _ptr(n), _ptr(parent), _ptr(token), _ptr(depth), _ptr(pos),
+          _ptr(rho), _ptr(mask), _ptr(ahat), _ptr(S), _ptr(S_curve), _ptr(dev_err), _stream(stream))
 
 
 @dataclass
@@ -262,10 +275,9 @@ def bastion_tree_attn(q, k_tree, v_tree, kv: KV, ctx_len, mask, n, out, scale: f
     if dev_err is not None:
         _need(dev_err, torch.int32, (1,), "dev_err")
     s = kv.c_struct()
-    _check(lib().bastion_tree_attn(_ptr(q), _ptr(k_tree), _ptr(v_tree), _dtype_code(q), B, N, Hq, Hkv, d,
-                                   float(scale), ctypes.byref(s), _ptr(ctx_len), _ptr(mask), _ptr(n), _ptr(out),
-                                   _ptr(ws), 0 if ws is None else ws.numel(), _ptr(dev_err), _stream(stream)),
-           "bastion_tree_attn")
+    _call("bastion_tree_attn", _ptr(q), _ptr(k_tree), _ptr(v_tree), _dtype_code(q), B, N, Hq, Hkv, d, float(scale),
+          ctypes.pointer(s), _ptr(ctx_len), _ptr(mask), _ptr(n), _ptr(out), _ptr(ws),
+          0 if ws is None else ws.numel(), _ptr(dev_err), _stream(stream))
 
 
 def bastion_accept_workspace_size(B: int, n_max: int) -> int:
@@ -291,10 +303,9 @@ def bastion_accept(target, n, parent, token, K: int, acc_len, acc_nodes, acc_tok
         _need(argmax_out, torch.int32, (B, N), "argmax_out")
     if dev_err is not None:
         _need(dev_err, torch.int32, (1,), "dev_err")
-    _check(lib().bastion_accept(_ptr(target), _dtype_code(target), B, N, V, row_stride, int(K), _ptr(n),
-                                _ptr(parent), _ptr(token), _ptr(acc_len), _ptr(acc_nodes), _ptr(acc_tok),
-                                _ptr(bonus), _ptr(argmax_out), _ptr(ws), ws.numel(), _ptr(dev_err),
-                                _stream(stream)), "bastion_accept")
+    _call("bastion_accept", _ptr(target), _dtype_code(target), B, N, V, row_stride, int(K), _ptr(n), _ptr(parent),
+          _ptr(token), _ptr(acc_len), _ptr(acc_nodes), _ptr(acc_tok), _ptr(bonus), _ptr(argmax_out), _ptr(ws),
+          ws.numel(), _ptr(dev_err), _stream(stream))
 
 
 def bastion_accept_noalloc(target, n, parent, token, K: int, acc_len, acc_nodes, acc_tok, bonus, argmax_out=None,
@@ -461,6 +472,37 @@ class SpecTreeStep:
     def __call__(self, logits, root_tok, ctx_len, C, L_AR, q, k_tree, v_tree, kv: KV, scale, target, stream=None):
         self.draft(logits, root_tok, ctx_len, C, L_AR, stream=stream)
         self.verify(q, k_tree, v_tree, kv, ctx_len, scale, target, stream=stream)
+
+    def prepare(self, logits, root_tok, ctx_len, C, L_AR, q, k_tree, v_tree, kv: KV, scale, target,
+                stream=None) -> "PreparedStep":
+        """Check and marshal the four calls of a step on these inputs once,
+        without launching anything; the returned object issues them on each
+        call.  Its stream is fixed now (``stream``, else the current one), and
+        it keeps the input tensors alive, whose contents may change between
+        calls but whose storage must not."""
+        if getattr(_rec, "calls", None) is not None:
+            raise BastionError("prepare() does not nest")
+        _rec.calls = []
+        try:
+            self(logits, root_tok, ctx_len, C, L_AR, q, k_tree, v_tree, kv, scale, target, stream=stream)
+            calls = _rec.calls
+        finally:
+            _rec.calls = None
+        return PreparedStep(calls, (self, logits, root_tok, ctx_len, C, q, k_tree, v_tree, kv, target))
+
+
+class PreparedStep:
+    """The four library calls of one spec-tree step with their arguments
+    already checked and marshalled (see ``SpecTreeStep.prepare``): calling it
+    only crosses the C ABI four times."""
+
+    def __init__(self, calls, keep):
+        self._calls = tuple(calls)
+        self._keep = keep   # the tensors whose device pointers the calls hold
+
+    def __call__(self) -> None:
+        for fn, args, name in self._calls:
+            _check(fn(*args), name)
 
 
 class HostStepRunner:
