@@ -43,6 +43,8 @@ constexpr int K1_WARPS = K1_THREADS / 32;
 constexpr int K1_CAP = 1024;                      // candidate buffer
 constexpr int K1_MAXC = 8;                        // CTAs per cluster (row), portable
 constexpr int K1_CHUNK_BYTES = 38 * 1024;         // preferred staged bytes per CTA (8 CTAs for a 152K bf16 row)
+constexpr int K1_CHUNK_BYTES_WAVES = 48 * 1024;   // when the clusters need more than one wave
+constexpr int K1_CTAS_PER_SM = 4;                 // the kernel's launch bound
 constexpr int K1_MAX_SMEM = 200 * 1024;           // largest chunk (very long rows)
 constexpr uint64_t K1_WAIT_NS = 200ull * 1000ull * 1000ull;
 
@@ -193,7 +195,7 @@ template <class Tag, bool kBulk>
 // at barriers and in their one staged copy, so more of them per SM keeps more
 // bytes in flight (measured: 15.5 -> 12.9 us on 64 rows of 151936, 35.9 ->
 // 33.0 us on 256 rows of 128256; a few bytes of spills).
-__global__ void __launch_bounds__(K1_THREADS, 4) topk_softmax_kernel(
+__global__ void __launch_bounds__(K1_THREADS, K1_CTAS_PER_SM) topk_softmax_kernel(
     const void *__restrict__ logits, int V, int64_t row_stride, int k, int chunk,
     int32_t *__restrict__ ids, float *__restrict__ lg, float *__restrict__ q, double *__restrict__ lse,
     uint32_t *__restrict__ dev_err) {
@@ -398,18 +400,25 @@ cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, 
                                 cudaStream_t stream) {
   const int esz = bf16 ? 2 : 4;
   const int vec = 16 / esz;
-  // CTAs per row: staged chunks of about 48 KB, at most a portable cluster of 8
-  // (very long rows take larger chunks)
+  // CTAs per row: staged chunks of about 38 KB, at most a portable cluster of 8
+  // (very long rows take larger chunks).  When the rows' clusters do not fit
+  // in one wave of resident CTAs, chunks of about 48 KB: fewer, longer CTAs
+  // take fewer waves (measured: 256 rows of 128256, 35.4 -> 33.3 us; 128 rows
+  // of 151936, 24.9 -> 24.2 us), while a single wave is faster with the
+  // smaller chunks (64 rows of 151936: 14.0 us against 14.5).
   const int64_t row_bytes = static_cast<int64_t>(V) * esz;
-  int C = static_cast<int>(std::min<int64_t>(K1_MAXC, (row_bytes + K1_CHUNK_BYTES - 1) / K1_CHUNK_BYTES));
-  if (C < 1) C = 1;
+  auto ctas_per_row = [&](int64_t chunk_bytes) {
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(K1_MAXC, (row_bytes + chunk_bytes - 1) / chunk_bytes)));
+  };
+  int C = ctas_per_row(K1_CHUNK_BYTES);
+  if (num_sms > 0 && static_cast<int64_t>(rows) * C > static_cast<int64_t>(K1_CTAS_PER_SM) * num_sms)
+    C = ctas_per_row(K1_CHUNK_BYTES_WAVES);
   int chunk = (V + C - 1) / C;
   chunk = (chunk + vec - 1) / vec * vec;
   C = (V + chunk - 1) / chunk;
   const bool bulk = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && ((row_stride * esz) % 16 == 0) &&
                     (row_bytes % 16 == 0) && (static_cast<int64_t>(chunk) * esz <= K1_MAX_SMEM);
 
-  (void)num_sms;
   const size_t dyn = bulk ? static_cast<size_t>(chunk) * esz : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, rows, 1);
