@@ -45,12 +45,12 @@ DEFAULT_WORKLOAD = "long_ctx_b4"
 # dram__bytes_write.sum, one capture of the workload); an entry counts only
 # while the kernel's sources still hash to `src`
 KNOWN_TRAFFIC = {
-    ("topk_softmax", "long_ctx_b4"): {"bytes": 19487488, "src": "5dd9b3a1da044c18"},
+    ("topk_softmax", "long_ctx_b4"): {"bytes": 19487488, "src": "b3ccdb7b481d15a2"},
     ("tree_attn", "long_ctx_b4"): {"bytes": 548102144, "src": "abb308e9ee576ad9"},
     ("accept", "long_ctx_b4"): {"bytes": 159599872, "src": "46cf3ac181492cfd"},
     ("tree_attn", "llama31_8b_b16_paged"): {"bytes": 295353856, "src": "abb308e9ee576ad9"},
     ("accept", "llama31_8b_b16_paged"): {"bytes": 50337024, "src": "46cf3ac181492cfd"},
-    ("topk_softmax", "qwen3_8b_b1"): {"bytes": 4905216, "src": "5dd9b3a1da044c18"},
+    ("topk_softmax", "qwen3_8b_b1"): {"bytes": 4905216, "src": "b3ccdb7b481d15a2"},
     ("tree_build", "qwen3_8b_b1"): {"bytes": 29440, "src": "48ae66f3c4acd9a7"},
     ("tree_attn", "qwen3_8b_b1"): {"bytes": 17634048, "src": "abb308e9ee576ad9"},
     ("accept", "qwen3_8b_b1"): {"bytes": 19477760, "src": "46cf3ac181492cfd"},

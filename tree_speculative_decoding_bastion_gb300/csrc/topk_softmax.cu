@@ -43,7 +43,7 @@ constexpr int K1_WARPS = K1_THREADS / 32;
 constexpr int K1_CAP = 1024;                      // candidate buffer
 constexpr int K1_MAXC = 8;                        // CTAs per cluster (row), portable
 constexpr int K1_CHUNK_BYTES = 38 * 1024;         // preferred staged bytes per CTA (8 CTAs for a 152K bf16 row)
-constexpr int K1_CHUNK_BYTES_WAVES = 48 * 1024;   // when the clusters need more than one wave
+constexpr int K1_CHUNK_BYTES_WAVES = 64 * 1024;   // when the clusters need more than one wave
 constexpr int K1_CTAS_PER_SM = 4;                 // the kernel's launch bound
 constexpr int K1_MAX_SMEM = 200 * 1024;           // largest chunk (very long rows)
 constexpr uint64_t K1_WAIT_NS = 200ull * 1000ull * 1000ull;
@@ -402,10 +402,11 @@ cudaError_t launch_topk_softmax(const void *logits, bool bf16, int rows, int V, 
   const int vec = 16 / esz;
   // CTAs per row: staged chunks of about 38 KB, at most a portable cluster of 8
   // (very long rows take larger chunks).  When the rows' clusters do not fit
-  // in one wave of resident CTAs, chunks of about 48 KB: fewer, longer CTAs
-  // take fewer waves (measured: 256 rows of 128256, 35.4 -> 33.3 us; 128 rows
-  // of 151936, 24.9 -> 24.2 us), while a single wave is faster with the
-  // smaller chunks (64 rows of 151936: 14.0 us against 14.5).
+  // in one wave of resident CTAs, chunks of up to 64 KB (three CTAs per SM):
+  // fewer, longer CTAs take fewer waves (measured: 256 rows of 128256,
+  // 35.4 -> 31.7 us with 64 KB, 33.3 with 48 KB; 128 rows of 151936,
+  // 24.9 -> 23.2 us), while a single wave is faster with the smaller chunks
+  // (64 rows of 151936: 14.0 us against 14.5 with 48 KB).
   const int64_t row_bytes = static_cast<int64_t>(V) * esz;
   auto ctas_per_row = [&](int64_t chunk_bytes) {
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(K1_MAXC, (row_bytes + chunk_bytes - 1) / chunk_bytes)));
